@@ -1,0 +1,359 @@
+"""Benchmark of one paged decode step on GB300.
+
+A step is the whole hot path for one batch: copy-on-write block copies (when
+the step has any), the append of each sequence's new token, and decode
+attention over every sequence's full context, for one attention layer.
+Default workload: Llama-3-8B geometry (32 q / 8 kv heads, d_h 128, bf16,
+16-token blocks), batch 64, lognormal(1024, 1.0) contexts clipped to
+[1, 8192], permuted pool with 10% free blocks.
+
+value = decode tokens per second = sequences per step / step time (all ranks'
+sequences over the slowest rank's time). Timing: CUDA events on the launch
+stream, L2 flushed (256 MiB write) before every timed step, outside the
+events. e2e: the same step through the public API from pinned host buffers,
+host->device copies of the step inputs and the device->host copy of the
+output inside the timed region.
+
+--impl reference times the oracle (plain numpy, float64) on a bounded sample
+of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention tokens/s and achieved HBM GB/s (% of GB300 peak)"
+UNIT = "tokens/s"
+L2_FLUSH_BYTES = 256 << 20
+KERNEL_SOURCE = os.path.join(ROOT, "paged_kv_cache_49_gb300", "csrc", "pkv_attn.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_dram_traffic.json")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama3_8b_b64")
+    ap.add_argument("--num-ctas", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_info():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def algorithmic_bytes(ctx, hq, hkv, d=128):
+    """Decode attention's bytes per launch: every context token's K and V
+    rows once, q and out, the table entries read and the lengths."""
+    ctx = np.asarray(ctx, dtype=np.int64)
+    kv = int(ctx.sum()) * hkv * d * 2 * 2
+    qo = 2 * len(ctx) * hq * d * 2
+    bt = int(((ctx + 15) // 16).sum()) * 4
+    return kv + qo + bt + len(ctx) * 4
+
+
+def measured_peak_gbs():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def kernel_hash():
+    with open(KERNEL_SOURCE, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(workload, units):
+    """DRAM bytes per launch from a committed ncu capture, scaled to this
+    launch by context tokens, or None if absent or the kernel changed."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if rec.get("kernel_sha256_16") != kernel_hash():
+        return None
+    if rec.get("workload") == workload:
+        return float(rec["dram_bytes_per_launch"])
+    if rec.get("context_tokens"):
+        return float(rec["dram_bytes_per_launch"]) * units / float(rec["context_tokens"])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples every 200 ms while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) >= 9:
+                        rows.append(parts)
+        finally:
+            os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def cpu_oracle_time(w, rows_budget_s=(10.0, 30.0)):
+    """The oracle's decode step (append + attention) on a sample of the
+    workload's sequences, repeated until at least rows_budget_s[0] seconds."""
+    from oracle import cache_ops, paged_attention, scenario
+
+    ref = scenario.replay(w, attend=False)
+    q, k_new, v_new = w.step_inputs()
+    k_pool, v_pool = ref["k_pool"], ref["v_pool"]
+    order = np.argsort(ref["ctx"])  # a spread of lengths: every 4th sequence by length
+    sample = sorted(order[::4].tolist())
+    done, t0 = 0, time.perf_counter()
+    while True:
+        cache_ops.append_kv(k_pool, v_pool, k_new[sample], v_new[sample], [ref["slots"][i] for i in sample])
+        paged_attention.paged_decode_attention(q, k_pool, v_pool, ref["tables"], ref["ctx"], w.scale, seqs=sample)
+        done += len(sample)
+        el = time.perf_counter() - t0
+        if el >= rows_budget_s[0] or el >= rows_budget_s[1]:
+            break
+    return {"value": done / el, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{len(sample)} of {w.batch_size} sequences (every 4th by context length, "
+                      f"{int(ref['ctx'][sample].sum())} context tokens), repeated for {el:.1f} s; "
+                      "numpy float64, single thread"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_info()
+    if rank != 0:
+        return
+    from workloads import make_workload
+    from oracle import cache_ops, paged_attention, scenario
+
+    w = make_workload(args.workload)
+    ref = scenario.replay(w, attend=False)
+    q, k_new, v_new = w.step_inputs()
+    order = np.argsort(ref["ctx"])
+    sample = sorted(order[::8].tolist())  # each step: every 8th sequence by length
+
+    def step():
+        cache_ops.append_kv(ref["k_pool"], ref["v_pool"], k_new[sample], v_new[sample],
+                            [ref["slots"][i] for i in sample])
+        paged_attention.paged_decode_attention(q, ref["k_pool"], ref["v_pool"], ref["tables"], ref["ctx"],
+                                               w.scale, seqs=sample)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    value = len(sample) * args.steps / el
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch_size, "q_heads": w.num_q_heads,
+                   "kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_tokens": 16,
+                   "sample_sequences": len(sample)},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{len(sample)} of {w.batch_size} sequences per step (every 8th by "
+                                   "context length); numpy float64, single thread"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    rank, world, local = dist_info()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    from paged_kv_cache_49_gb300 import build
+    if rank == 0 or world == 1:
+        build.build()
+    if world > 1:
+        dist.barrier()
+    import paged_kv_cache_49_gb300 as pkv
+    from workloads import make_workload
+
+    # Weak scaling: every rank serves its own independent batch (seed = rank).
+    w = make_workload(args.workload, seed=rank)
+    eng = pkv.PagedKVEngine(w.pool_blocks, w.num_q_heads, w.num_kv_heads, w.head_dim, free_order=w.free_order)
+    eng.load_workload_pool(w)
+    eng.replay_events(w, with_content=True)
+    q_bits, k_bits, v_bits = w.step_inputs()
+    sb = eng.prepare_step(w.batch, q_bits, k_bits, v_bits)
+    ctx = sb.ctx.cpu().numpy()
+    B = w.batch_size
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+
+    for _ in range(args.warmup):
+        eng.run_step(sb, w.scale, args.num_ctas)
+    torch.cuda.synchronize()
+    if eng.read_errors(sb):
+        raise RuntimeError("device error word set during warm-up")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            ev[i][0].record(stream)
+            if sb.num_pairs:
+                pkv.block_copy(eng.k_cache, eng.v_cache, sb.pairs, eng.error)
+            pkv.append(sb.k, sb.v, sb.slots, eng.k_cache, eng.v_cache, eng.error)
+            ev[i][1].record(stream)
+            pkv.attn_decode(sb.q, eng.k_cache, eng.v_cache, sb.tables, sb.ctx, w.scale, sb.out,
+                            sb.workspace, args.num_ctas)
+            ev[i][2].record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    step_ms = [e[0].elapsed_time(e[2]) for e in ev]
+    attn_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    ms = statistics.mean(step_ms)
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = B * world / (ms * 1e-3)
+    launches = args.steps * (2 + (1 if sb.num_pairs else 0))
+    if eng.read_errors(sb):
+        raise RuntimeError("device error word set during the timed steps")
+
+    # ---- end to end through the public API from pinned host buffers ----
+    e2e = None
+    if not args.no_e2e:
+        host = {name: getattr(sb, name).cpu().pin_memory()
+                for name in ("q", "k", "v", "slots", "pairs", "tables", "ctx")}
+        out_host = torch.empty(sb.out.shape, dtype=sb.out.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = out_host.numel() * out_host.element_size()
+        ees = []
+        for i in range(args.warmup + args.steps):
+            flush.fill_(i & 0xFF)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for name, t in host.items():
+                getattr(sb, name).copy_(t, non_blocking=True)
+            eng.run_step(sb, w.scale, args.num_ctas)
+            out_host.copy_(sb.out, non_blocking=True)
+            e1.record(stream)
+            e1.synchronize()
+            if i >= args.warmup:
+                ees.append(e0.elapsed_time(e1))
+        e2e_ms = statistics.mean(ees)
+        if world > 1:
+            t = torch.tensor([e2e_ms], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": B * world / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    abytes = algorithmic_bytes(ctx, w.num_q_heads, w.num_kv_heads)
+    attn_s = statistics.mean(attn_ms) * 1e-3
+    peak, peak_kind = measured_peak_gbs()
+    achieved = abytes / attn_s / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": recorded_traffic(w.name, int(ctx.sum())),
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs copy bandwidth)",
+                "kernel": "pkv::attn::decode_kernel", "algorithmic_bytes_per_launch": abytes,
+                "attn_ms": attn_s * 1e3, "frac_of_nominal_8tbs": achieved / 8000.0}
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        cpu = cpu_oracle_time(w)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "batch": B, "q_heads": w.num_q_heads, "kv_heads": w.num_kv_heads,
+                   "head_dim": w.head_dim, "block_tokens": 16, "context_tokens": int(ctx.sum()),
+                   "pool_blocks": w.pool_blocks, "cow_pairs_per_step": sb.num_pairs,
+                   "num_ctas": args.num_ctas or pkv.default_ctas(), "l2": "flushed (256 MiB write) before each step",
+                   "parallelism": f"replicas x{world}"},
+        "clocks": clk.summary(), "e2e": e2e, "gpu_launches": launches, "roofline": roofline,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,266 @@
+/*
+ * pkv.h -- C ABI of libpkv: paged KV cache decode on GB300 (sm_103a).
+ *
+ * The KV cache of one attention layer is a preallocated pool of fixed-size
+ * blocks of 16 tokens; each sequence reaches its tokens through a block table
+ * that maps logical block i to a physical block id (cs2680 Lecture 10, §10.3
+ * "PagedAttention: the KV cache as virtual memory"; "The inference server":
+ * the KV cache is one arena allocated at start-up, with no allocator on the
+ * hot path).
+ *
+ * Device-side layout (all bf16 buffers hold IEEE bfloat16 values, row-major):
+ *   k_cache, v_cache : [num_blocks][num_kv_heads][16][head_dim]
+ *                      token t of a sequence, KV head g, lives at
+ *                      [table[t / 16]][g][t % 16][:]
+ *   q, out           : [num_seqs][num_q_heads][head_dim]
+ *   k, v (append)    : [num_tokens][num_kv_heads][head_dim]
+ *   block_tables     : int32 [num_seqs][max_blocks_per_seq]; entries past
+ *                      ceil(context_len / 16) in a row are never read
+ *   context_lens     : int32 [num_seqs]
+ *   slot_mapping     : int64 [num_tokens]; slot = block * 16 + (pos % 16)
+ *   src_dst_pairs    : int32 [num_pairs][2]
+ * Query head h uses KV head h / (num_q_heads / num_kv_heads).
+ *
+ * Ownership: the caller owns every device buffer and stream; the library
+ * allocates no device memory and frees nothing it did not create. Every
+ * device call is asynchronous on the given stream (a cudaStream_t passed as
+ * void*; NULL = the legacy default stream) and returns after the launch.
+ *
+ * Errors: calls return a pkv_status. Argument errors found on the host return
+ * before anything is launched. Errors that only the device can see (a block
+ * id or slot outside the pool, a context longer than its table row, a bounded
+ * wait that ran out) never fault the GPU: the kernel skips the access, ORs a
+ * PKV_DEVERR_* bit into a device-side 32-bit error word, and carries on; the
+ * host reads that word with pkv_read_device_error.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int pkv_status;
+
+#define PKV_OK 0
+#define PKV_EINVAL (-1)      /* bad argument (null pointer, shape, alignment) */
+#define PKV_ENOMEM (-2)      /* too few free pages: admission or fork refused */
+#define PKV_ERANGE (-3)      /* id or length outside the valid range */
+#define PKV_ECUDA (-4)       /* a CUDA runtime call failed */
+#define PKV_ENOSPC (-5)      /* append past the pages a sequence reserved */
+#define PKV_EUNSUPPORTED (-6) /* geometry this build does not handle */
+#define PKV_ESTATE (-7)      /* block manager found its own state inconsistent */
+
+/* Bits of the device-side error word. */
+#define PKV_DEVERR_BLOCK_ID 0x1u  /* block id outside [0, num_blocks) in a table or pair */
+#define PKV_DEVERR_SLOT 0x2u      /* slot outside [0, num_blocks * 16) */
+#define PKV_DEVERR_CONTEXT 0x4u   /* context_len > 16 * max_blocks_per_seq */
+#define PKV_DEVERR_TIMEOUT 0x8u   /* an internal wait gave up; the output is invalid */
+
+#define PKV_BLOCK_TOKENS 16
+#define PKV_ATTN_HEAD_DIM 128   /* head_dim of pkv_attn_decode */
+#define PKV_ATTN_MAX_GROUP 8    /* max num_q_heads / num_kv_heads */
+#define PKV_ATTN_MAX_SEQS 4096  /* max num_seqs of one pkv_attn_decode call */
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+int pkv_version(void);
+
+/* Static description of a status code. */
+const char* pkv_status_string(pkv_status status);
+
+/* Message of the last CUDA error seen by this thread inside the library. */
+const char* pkv_last_cuda_error(void);
+
+/* Copy the device error word to *host_value (synchronises the stream); if
+ * clear != 0, reset it to zero afterwards. */
+pkv_status pkv_read_device_error(uint32_t* device_error, uint32_t* host_value,
+                                 int clear, void* stream);
+
+/*
+ * pkv_append -- write each new token's K and V into its cache slot.
+ *
+ * cs2680 Lecture 10, §10.3: a sequence grows by one token by writing one slot
+ * of its last block (or of the next block it owns); the slot is
+ * table[pos / 16] * 16 + pos % 16, computed on the host by
+ * pkv_bm_prepare_append.
+ *   k, v          : device bf16 [num_tokens][num_kv_heads][head_dim]
+ *   slot_mapping  : device int64 [num_tokens]; a negative slot marks a padding
+ *                   row and writes nothing ("The inference server": padding
+ *                   rows of a bucketed batch are discarded)
+ *   k_cache, v_cache : device bf16 pool, layout above
+ *   device_error  : device uint32 error word, or NULL
+ * Slots must be distinct (two rows writing one slot race). head_dim must be a
+ * multiple of 8; every bf16 pointer 16-byte aligned. A slot >= num_blocks * 16
+ * is skipped and sets PKV_DEVERR_SLOT.
+ */
+pkv_status pkv_append(const void* k, const void* v, const int64_t* slot_mapping,
+                      int num_tokens, void* k_cache, void* v_cache, int num_blocks,
+                      int num_kv_heads, int head_dim, uint32_t* device_error,
+                      void* stream);
+
+/*
+ * pkv_block_copy -- copy-on-write of whole blocks.
+ *
+ * "KV cache systems", copy-on-write paragraph, and cs2680 Lecture 10, §10.4:
+ * the first writer of a shared block gets a private copy of it. For each pair
+ * (src, dst), physical block dst of both caches becomes a copy of block src
+ * (all KV heads, all 16 rows). Destinations must be distinct and no
+ * destination may also be a source in the same call. Pairs with an id
+ * outside [0, num_blocks) are skipped and set PKV_DEVERR_BLOCK_ID.
+ *   src_dst_pairs : device int32 [num_pairs][2]
+ */
+pkv_status pkv_block_copy(void* k_cache, void* v_cache, const int32_t* src_dst_pairs,
+                          int num_pairs, int num_blocks, int num_kv_heads, int head_dim,
+                          uint32_t* device_error, void* stream);
+
+/*
+ * pkv_attn_workspace_size -- bytes of device scratch pkv_attn_decode needs for
+ * num_seqs sequences and num_kv_heads KV heads on the current device.
+ * The workspace holds the error word (its first 4 bytes), one counter per
+ * (sequence, KV head) and two fp32 partial results per CTA. Returns 0 for
+ * invalid arguments or when no device is present.
+ */
+size_t pkv_attn_workspace_size(int num_seqs, int num_kv_heads);
+
+/* Zero a workspace (asynchronously, on stream). Needed once after it is
+ * allocated, and again after a call that set PKV_DEVERR_TIMEOUT; every
+ * pkv_attn_decode leaves its counters at zero. */
+pkv_status pkv_attn_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * pkv_attn_decode -- single-token decode attention through block tables.
+ *
+ * For every sequence s and query head h (KV head g = h / (Hq / Hkv)):
+ *   x_t = scale * <q[s,h], K[table[s][t/16]][g][t%16]>,  t < context_lens[s]
+ *   out[s,h] = sum_t softmax(x)_t * V[table[s][t/16]][g][t%16]
+ * (cs2680 Lecture 10, §10.3, step three: attention reads through the block
+ * table, with the same FLOPs and bytes as over a contiguous cache; "The
+ * inference server": attention takes a block table and a length tensor, both
+ * fixed-shape, so growth changes values, not shapes.)
+ * bf16 inputs and output, fp32 accumulation and softmax; the output is
+ * rounded to nearest even. context_lens[s] <= 0 gives a zero output row.
+ *   q, out        : device bf16 [num_seqs][num_q_heads][128]
+ *   block_tables  : device int32 [num_seqs][max_blocks_per_seq]
+ *   context_lens  : device int32 [num_seqs]
+ *   num_ctas      : number of persistent CTAs, 0 = as many as fit at once on
+ *                   the device; the context of all (sequence, KV head) pairs
+ *                   is split evenly among them and partial results of a pair
+ *                   split across CTAs are merged in the same launch
+ *   workspace     : device scratch of at least
+ *                   pkv_attn_workspace_size(num_seqs, num_kv_heads) bytes,
+ *                   zeroed once by pkv_attn_workspace_init; its first 4 bytes
+ *                   are the device error word. Calls that share a workspace
+ *                   must not overlap on the GPU.
+ * Limits: head_dim == 128, num_q_heads % num_kv_heads == 0,
+ * num_q_heads / num_kv_heads <= 8, 1 <= num_seqs <= 4096,
+ * num_blocks * num_kv_heads * 16 < 2^31. A block id outside [0, num_blocks)
+ * is never dereferenced: block 0 is read in its place and PKV_DEVERR_BLOCK_ID
+ * is set (the output is then invalid); context_lens above
+ * 16 * max_blocks_per_seq are clamped and set PKV_DEVERR_CONTEXT.
+ */
+pkv_status pkv_attn_decode(const void* q, const void* k_cache, const void* v_cache,
+                           const int32_t* block_tables, int max_blocks_per_seq,
+                           const int32_t* context_lens, int num_seqs, int num_q_heads,
+                           int num_kv_heads, int head_dim, int num_blocks, float scale,
+                           int num_ctas, void* workspace, size_t workspace_bytes,
+                           void* out, void* stream);
+
+/* Number of persistent CTAs pkv_attn_decode launches when num_ctas == 0. */
+int pkv_attn_default_ctas(void);
+
+/* ---------------------------------------------------------------------------
+ * Host block manager.
+ *
+ * Owns the free list, the per-block reference counts and each sequence's
+ * block table; it never touches device memory (freeing a sequence changes
+ * ownership only -- "Reserve the page a request has not written yet",
+ * "Separate the pool from its owners").
+ *
+ * Policy:
+ *  - admission reserves ceil((prompt_len + max_new) / 16) pages at once and
+ *    is refused (PKV_ENOMEM, no state change) when fewer pages are free
+ *    ("Pick a reservation policy you can explain"); every call that changes
+ *    state runs under one mutex, so reserve-and-admit is one decision even
+ *    with concurrent callers;
+ *  - members of a prefix group share the complete pages of their common
+ *    prefix (prefix_len / 16 pages, charged once); the rest of each
+ *    request's reservation is private ("Charge shared pages once");
+ *  - fork: children share the parent's written blocks by reference count
+ *    (cs2680 Lecture 10, §10.4); each child reserves private pages for the
+ *    rest of its allowance and, when the parent's last written block is
+ *    partial, one spare page for the copy-on-write of that block;
+ *  - copy-on-write: a sequence that writes into a block with refcount > 1
+ *    takes a spare page as its own copy and reports the (src, dst) pair; a
+ *    writer that sees refcount 1 writes in place ("KV cache systems",
+ *    copy-on-write paragraph);
+ *  - free pages are handed out in free_order (ascending ids if NULL); a
+ *    released page is the next one handed out.
+ * A call that returns an error changes no state.
+ * ------------------------------------------------------------------------- */
+typedef struct pkv_bm pkv_bm;
+
+typedef struct pkv_bm_stats_t {
+    int32_t num_blocks;
+    int32_t free_blocks;   /* on the free list */
+    int32_t used_blocks;   /* refcount > 0 */
+    int32_t shared_blocks; /* refcount > 1 */
+    int32_t spare_blocks;  /* reserved for a future copy-on-write */
+    int32_t num_seqs;
+    int64_t ref_sum;       /* sum of refcounts == sum of table lengths */
+    int64_t cow_copies;    /* copy-on-write pairs reported so far */
+} pkv_bm_stats_t;
+
+/* free_order: host int32 permutation of [0, num_blocks), or NULL. Returns NULL
+ * on invalid arguments. block_tokens must be 16. */
+pkv_bm* pkv_bm_create(int num_blocks, int block_tokens, const int32_t* free_order);
+void pkv_bm_destroy(pkv_bm* bm);
+
+/* group < 0: no sharing (prefix_len ignored). group >= 0: 0 <= prefix_len <=
+ * prompt_len, and every member of a group must pass the same prefix_len. The
+ * sequence starts with context length prompt_len (its prompt KV is written by
+ * prefill, outside this library). */
+pkv_status pkv_bm_admit(pkv_bm* bm, int prompt_len, int max_new, int group,
+                        int prefix_len, int* seq_id);
+
+/* child_ids: host int32 [n]. All-or-nothing. */
+pkv_status pkv_bm_fork(pkv_bm* bm, int parent_seq, int n, int32_t* child_ids);
+
+/* For each listed sequence (distinct ids, processed in order): the slot of
+ * its next token and, where that token lands in a shared block, one
+ * copy-on-write pair; then its context length grows by one.
+ *   slot_mapping_out : host int64 [n]
+ *   cow_pairs_out    : host int32 [n][2] (at most one pair per sequence)
+ *   n_pairs_out      : number of pairs written
+ * PKV_ENOSPC if a sequence has no reserved slot left (nothing changes). */
+pkv_status pkv_bm_prepare_append(pkv_bm* bm, const int32_t* seq_ids, int n,
+                                 int64_t* slot_mapping_out, int32_t* cow_pairs_out,
+                                 int* n_pairs_out);
+
+pkv_status pkv_bm_free(pkv_bm* bm, int seq_id);
+
+/* Block table of one sequence into out[0 .. capacity); *length = its length.
+ * PKV_ERANGE if capacity is too small. */
+pkv_status pkv_bm_block_table(pkv_bm* bm, int seq_id, int32_t* out, int capacity,
+                              int* length);
+
+pkv_status pkv_bm_context_len(pkv_bm* bm, int seq_id, int* context_len);
+
+/* Padded batch view: tables_out int32 [n][width] (unused entries -1) and
+ * context_lens_out int32 [n], ready to copy to the device for
+ * pkv_attn_decode. PKV_ERANGE if a table is longer than width. */
+pkv_status pkv_bm_batch_tables(pkv_bm* bm, const int32_t* seq_ids, int n,
+                               int32_t* tables_out, int width, int32_t* context_lens_out);
+
+pkv_status pkv_bm_stats(pkv_bm* bm, pkv_bm_stats_t* stats);
+
+/* Reference count of a physical block (-1 if out of range). */
+int pkv_bm_refcount(pkv_bm* bm, int block);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

@@ -1,0 +1,14 @@
+"""GB300-native paged KV cache decode.
+
+libpkv (C ABI, include/pkv.h) holds the CUDA kernels for sm_103a -- paged
+decode attention, KV append, copy-on-write block copy -- and the C++ host
+block manager. This package is the thin Python binding over it plus a small
+engine that drives one attention layer's pool.
+"""
+from ._native import (  # noqa: F401
+    BLOCK_TOKENS, DEVERR_BLOCK_ID, DEVERR_CONTEXT, DEVERR_SLOT, DEVERR_TIMEOUT, EXPORTED,
+    HEAD_DIM, LIB_PATH, MAX_GROUP, AttentionWorkspace, BlockManager, PkvError, PoolExhausted,
+    ReservationExceeded, append, attn_decode, block_copy, default_ctas, new_error_word,
+    read_device_error,
+)
+from .engine import PagedKVEngine, StepBuffers, bf16_from_bits, bits_from_bf16  # noqa: F401

@@ -1,0 +1,330 @@
+"""ctypes binding of libpkv (include/pkv.h): argument marshalling only.
+
+Every operation runs in the library's CUDA kernels or its C++ block manager;
+torch is used for device memory, streams and dtype views. Importing this
+module fails loudly if libpkv.so has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpkv.so")
+
+PKV_OK = 0
+PKV_EINVAL = -1
+PKV_ENOMEM = -2
+PKV_ERANGE = -3
+PKV_ECUDA = -4
+PKV_ENOSPC = -5
+PKV_EUNSUPPORTED = -6
+PKV_ESTATE = -7
+
+DEVERR_BLOCK_ID = 0x1
+DEVERR_SLOT = 0x2
+DEVERR_CONTEXT = 0x4
+DEVERR_TIMEOUT = 0x8
+
+BLOCK_TOKENS = 16
+HEAD_DIM = 128
+MAX_GROUP = 8
+MAX_SEQS = 4096
+
+EXPORTED = [
+    "pkv_version", "pkv_status_string", "pkv_last_cuda_error", "pkv_read_device_error",
+    "pkv_append", "pkv_block_copy", "pkv_attn_workspace_size", "pkv_attn_workspace_init",
+    "pkv_attn_decode", "pkv_attn_default_ctas", "pkv_bm_create", "pkv_bm_destroy",
+    "pkv_bm_admit", "pkv_bm_fork", "pkv_bm_prepare_append", "pkv_bm_free",
+    "pkv_bm_block_table", "pkv_bm_context_len", "pkv_bm_batch_tables", "pkv_bm_stats",
+    "pkv_bm_refcount",
+]
+
+
+class PkvError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        msg = _lib.pkv_status_string(status).decode()
+        if status == PKV_ECUDA:
+            msg += f" ({_lib.pkv_last_cuda_error().decode()})"
+        super().__init__(f"{what}: {msg} [{status}]" if what else f"{msg} [{status}]")
+
+
+class PoolExhausted(PkvError):
+    pass
+
+
+class ReservationExceeded(PkvError):
+    pass
+
+
+class StatsT(ctypes.Structure):
+    _fields_ = [
+        ("num_blocks", ctypes.c_int32), ("free_blocks", ctypes.c_int32),
+        ("used_blocks", ctypes.c_int32), ("shared_blocks", ctypes.c_int32),
+        ("spare_blocks", ctypes.c_int32), ("num_seqs", ctypes.c_int32),
+        ("ref_sum", ctypes.c_int64), ("cow_copies", ctypes.c_int64),
+    ]
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build it with `python paged_kv_cache_49_gb300/build.py` "
+            "(nvcc for sm_103a); there is no fallback implementation")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+    f32 = ctypes.c_float
+    sig = {
+        "pkv_version": (i32, []),
+        "pkv_status_string": (ctypes.c_char_p, [i32]),
+        "pkv_last_cuda_error": (ctypes.c_char_p, []),
+        "pkv_read_device_error": (i32, [vp, vp, i32, vp]),
+        "pkv_append": (i32, [vp, vp, vp, i32, vp, vp, i32, i32, i32, vp, vp]),
+        "pkv_block_copy": (i32, [vp, vp, vp, i32, i32, i32, i32, vp, vp]),
+        "pkv_attn_workspace_size": (sz, [i32, i32]),
+        "pkv_attn_workspace_init": (i32, [vp, sz, vp]),
+        "pkv_attn_decode": (i32, [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, f32, i32, vp, sz, vp, vp]),
+        "pkv_attn_default_ctas": (i32, []),
+        "pkv_bm_create": (vp, [i32, i32, vp]),
+        "pkv_bm_destroy": (None, [vp]),
+        "pkv_bm_admit": (i32, [vp, i32, i32, i32, i32, vp]),
+        "pkv_bm_fork": (i32, [vp, i32, i32, vp]),
+        "pkv_bm_prepare_append": (i32, [vp, vp, i32, vp, vp, vp]),
+        "pkv_bm_free": (i32, [vp, i32]),
+        "pkv_bm_block_table": (i32, [vp, i32, vp, i32, vp]),
+        "pkv_bm_context_len": (i32, [vp, i32, vp]),
+        "pkv_bm_batch_tables": (i32, [vp, vp, i32, vp, i32, vp]),
+        "pkv_bm_stats": (i32, [vp, vp]),
+        "pkv_bm_refcount": (i32, [vp, i32]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    del i64
+    return lib
+
+
+_lib = _load()
+lib = _lib
+
+
+def _check(status: int, what: str) -> None:
+    if status == PKV_OK:
+        return
+    if status == PKV_ENOMEM:
+        raise PoolExhausted(status, what)
+    if status == PKV_ENOSPC:
+        raise ReservationExceeded(status, what)
+    raise PkvError(status, what)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _need(t: torch.Tensor, dtype, name: str, cuda: bool = True) -> None:
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if cuda and not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+# ---------------------------------------------------------------------------
+# device operations
+
+
+def new_error_word(device=None) -> torch.Tensor:
+    """A zeroed device uint32 error word (held as int32) for append / copy."""
+    return torch.zeros(1, dtype=torch.int32, device=device or "cuda")
+
+
+def read_device_error(word: torch.Tensor, clear: bool = True, stream=None) -> int:
+    host = ctypes.c_uint32(0)
+    _check(_lib.pkv_read_device_error(_ptr(word), ctypes.byref(host), int(clear), _stream(stream)),
+           "pkv_read_device_error")
+    return host.value
+
+
+def append(k, v, slot_mapping, k_cache, v_cache, device_error=None, stream=None) -> None:
+    """Write k[i], v[i] ([T, Hkv, D] bf16) into slot slot_mapping[i] (int64)."""
+    _need(k, torch.bfloat16, "k")
+    _need(v, torch.bfloat16, "v")
+    _need(slot_mapping, torch.int64, "slot_mapping")
+    _need(k_cache, torch.bfloat16, "k_cache")
+    _need(v_cache, torch.bfloat16, "v_cache")
+    nb, hkv, bt, d = k_cache.shape
+    if v_cache.shape != k_cache.shape or bt != BLOCK_TOKENS:
+        raise ValueError("caches must be [num_blocks, Hkv, 16, D] and alike")
+    T = slot_mapping.numel()
+    if k.shape != (T, hkv, d) or v.shape != (T, hkv, d):
+        raise ValueError("k, v must be [T, Hkv, D] matching the cache and slot_mapping")
+    _check(_lib.pkv_append(_ptr(k), _ptr(v), _ptr(slot_mapping), T, _ptr(k_cache), _ptr(v_cache),
+                           nb, hkv, d, _ptr(device_error), _stream(stream)), "pkv_append")
+
+
+def block_copy(k_cache, v_cache, pairs, device_error=None, stream=None) -> None:
+    """Copy physical block pairs[i, 0] onto pairs[i, 1] in both caches."""
+    _need(k_cache, torch.bfloat16, "k_cache")
+    _need(v_cache, torch.bfloat16, "v_cache")
+    _need(pairs, torch.int32, "pairs")
+    nb, hkv, bt, d = k_cache.shape
+    n = pairs.shape[0] if pairs.numel() else 0
+    if n and pairs.shape != (n, 2):
+        raise ValueError("pairs must be [n, 2]")
+    _check(_lib.pkv_block_copy(_ptr(k_cache), _ptr(v_cache), _ptr(pairs) if n else None, n, nb, hkv, d,
+                               _ptr(device_error), _stream(stream)), "pkv_block_copy")
+
+
+def default_ctas() -> int:
+    return int(_lib.pkv_attn_default_ctas())
+
+
+class AttentionWorkspace:
+    """Device scratch for attn_decode: error word, per-(seq, KV head) counters
+    and per-CTA partials, zeroed once at creation."""
+
+    def __init__(self, num_seqs: int, num_kv_heads: int, device=None, stream=None):
+        nbytes = int(_lib.pkv_attn_workspace_size(num_seqs, num_kv_heads))
+        if nbytes == 0:
+            raise PkvError(PKV_EINVAL, "pkv_attn_workspace_size")
+        self.num_seqs, self.num_kv_heads, self.nbytes = num_seqs, num_kv_heads, nbytes
+        self.buffer = torch.empty(nbytes + 256, dtype=torch.uint8, device=device or "cuda")
+        off = (-self.buffer.data_ptr()) % 256
+        self.tensor = self.buffer[off : off + nbytes]
+        _check(_lib.pkv_attn_workspace_init(self.tensor.data_ptr(), nbytes, _stream(stream)),
+               "pkv_attn_workspace_init")
+
+    @property
+    def ptr(self) -> int:
+        return self.tensor.data_ptr()
+
+    def error_word(self) -> torch.Tensor:
+        return self.tensor[:4].view(torch.int32)
+
+    def read_error(self, clear: bool = True, stream=None) -> int:
+        return read_device_error(self.error_word(), clear, stream)
+
+
+def attn_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out=None, workspace=None,
+                num_ctas: int = 0, stream=None):
+    """Decode attention through block tables; returns out [B, Hq, 128] bf16."""
+    _need(q, torch.bfloat16, "q")
+    _need(k_cache, torch.bfloat16, "k_cache")
+    _need(v_cache, torch.bfloat16, "v_cache")
+    _need(block_tables, torch.int32, "block_tables")
+    _need(context_lens, torch.int32, "context_lens")
+    B, hq, d = q.shape
+    nb, hkv, bt, d2 = k_cache.shape
+    if d != d2 or v_cache.shape != k_cache.shape or bt != BLOCK_TOKENS:
+        raise ValueError("q [B, Hq, D] and caches [NB, Hkv, 16, D] must agree")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or context_lens.shape != (B,):
+        raise ValueError("block_tables must be [B, W] and context_lens [B]")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, torch.bfloat16, "out")
+    if workspace is None:
+        workspace = AttentionWorkspace(B, hkv, device=q.device, stream=stream)
+    _check(_lib.pkv_attn_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                block_tables.shape[1], _ptr(context_lens), B, hq, hkv, d, nb,
+                                float(scale), int(num_ctas), workspace.ptr, workspace.nbytes,
+                                _ptr(out), _stream(stream)), "pkv_attn_decode")
+    return out
+
+
+# ---------------------------------------------------------------------------
+# host block manager
+
+
+class BlockManager:
+    """Free list, refcounts, copy-on-write and page-rounded admission (C++)."""
+
+    def __init__(self, num_blocks: int, block_tokens: int = BLOCK_TOKENS, free_order=None):
+        order = None
+        self._order_buf = None
+        if free_order is not None:
+            arr = (ctypes.c_int32 * num_blocks)(*[int(x) for x in free_order])
+            self._order_buf = arr
+            order = ctypes.cast(arr, ctypes.c_void_p)
+        self._h = _lib.pkv_bm_create(num_blocks, block_tokens, order)
+        if not self._h:
+            raise PkvError(PKV_EINVAL, "pkv_bm_create")
+        self.num_blocks = num_blocks
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h:
+            _lib.pkv_bm_destroy(h)
+            self._h = None
+
+    def admit(self, prompt_len: int, max_new: int, group: int = -1, prefix_len: int = 0) -> int:
+        sid = ctypes.c_int(0)
+        _check(_lib.pkv_bm_admit(self._h, prompt_len, max_new, group, prefix_len, ctypes.byref(sid)),
+               "pkv_bm_admit")
+        return sid.value
+
+    def fork(self, parent: int, n: int) -> list[int]:
+        ids = (ctypes.c_int32 * max(n, 1))()
+        _check(_lib.pkv_bm_fork(self._h, parent, n, ids), "pkv_bm_fork")
+        return list(ids[:n])
+
+    def prepare_append(self, seq_ids):
+        """Returns (slots list[int], pairs list[(src, dst)])."""
+        n = len(seq_ids)
+        ids = (ctypes.c_int32 * max(n, 1))(*seq_ids)
+        slots = (ctypes.c_int64 * max(n, 1))()
+        pairs = (ctypes.c_int32 * max(2 * n, 2))()
+        npairs = ctypes.c_int(0)
+        _check(_lib.pkv_bm_prepare_append(self._h, ids, n, slots, pairs, ctypes.byref(npairs)),
+               "pkv_bm_prepare_append")
+        return list(slots[:n]), [(pairs[2 * i], pairs[2 * i + 1]) for i in range(npairs.value)]
+
+    def free(self, seq_id: int) -> None:
+        _check(_lib.pkv_bm_free(self._h, seq_id), "pkv_bm_free")
+
+    def table(self, seq_id: int) -> list[int]:
+        length = ctypes.c_int(0)
+        st = _lib.pkv_bm_block_table(self._h, seq_id, None, 0, ctypes.byref(length))
+        if st not in (PKV_OK, PKV_ERANGE):
+            _check(st, "pkv_bm_block_table")
+        buf = (ctypes.c_int32 * max(length.value, 1))()
+        _check(_lib.pkv_bm_block_table(self._h, seq_id, buf, length.value, ctypes.byref(length)),
+               "pkv_bm_block_table")
+        return list(buf[: length.value])
+
+    def context_len(self, seq_id: int) -> int:
+        c = ctypes.c_int(0)
+        _check(_lib.pkv_bm_context_len(self._h, seq_id, ctypes.byref(c)), "pkv_bm_context_len")
+        return c.value
+
+    def batch_tables(self, seq_ids, width: int):
+        """(tables int32 [n, width] with -1 padding, context_lens int32 [n]) as CPU tensors."""
+        n = len(seq_ids)
+        ids = (ctypes.c_int32 * max(n, 1))(*seq_ids)
+        tables = torch.empty((n, width), dtype=torch.int32)
+        ctx = torch.empty((n,), dtype=torch.int32)
+        _check(_lib.pkv_bm_batch_tables(self._h, ids, n, tables.data_ptr(), width, ctx.data_ptr()),
+               "pkv_bm_batch_tables")
+        return tables, ctx
+
+    def stats(self) -> dict:
+        s = StatsT()
+        _check(_lib.pkv_bm_stats(self._h, ctypes.byref(s)), "pkv_bm_stats")
+        return {"free": s.free_blocks, "used": s.used_blocks, "shared": s.shared_blocks,
+                "ref_sum": s.ref_sum, "spares": s.spare_blocks, "cow_copies": s.cow_copies,
+                "seqs": s.num_seqs}
+
+    def refcount(self, block: int) -> int:
+        return int(_lib.pkv_bm_refcount(self._h, block))

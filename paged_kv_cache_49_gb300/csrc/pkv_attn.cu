@@ -1,0 +1,708 @@
+// Paged decode attention for sm_103a.
+//
+// What it computes (cs2680 Lecture 10, §10.3, step three; "KV cache systems",
+// block-table indirection paragraph): for every sequence s and query head h,
+// softmax(scale * q[s,h] . K_t) weighted sum of V_t over the sequence's
+// context, where token t lives in physical block table[s][t / 16], row t % 16.
+//
+// How (GB300 design):
+//  * Work split. The context of every (sequence, KV head) pair is a run of
+//    16-token blocks; all runs are laid end to end, in (sequence, KV head)
+//    order, and the whole line is cut into gridDim.x equal ranges, one per
+//    persistent CTA. Every CTA derives the same split on the device from
+//    context_lens (a prefix sum over sequences), so the call needs no
+//    host-side knowledge of the lengths and is balanced to within one block
+//    whatever the length mix. A pair cut by a range boundary becomes two or
+//    more pieces; each piece leaves an fp32 partial (max, sum, unnormalised
+//    output) and the CTA that finishes a pair's last piece merges them with a
+//    log-sum-exp rescale ("last arrival merges": one atomic counter per pair,
+//    no waiting on other CTAs, reset by the merger).
+//  * Data movement. One producer warp walks the range, reads block ids from
+//    the table, and issues TMA tile loads (two 16 x 64 bf16 boxes per 4 KiB K
+//    or V block, 128-byte swizzle, L2 evict-first) into an 8-stage ring of
+//    shared memory, each stage one block of K and V. The query rows of a
+//    piece arrive by one bulk copy into a 4-slot ring.
+//  * Math. Four consumer warps take the ring's blocks round robin. Per block:
+//    S^T[16 tokens x 8 heads] = K Q^T on the tensor cores (mma.sync m16n8k16,
+//    bf16 in, fp32 out, K fragments by ldmatrix from the swizzled stage), an
+//    online softmax in fp32 (max over tokens by shuffles, exp2 in the log2
+//    domain), P cast to bf16 and transposed in registers (movmatrix), then
+//    O^T[128 dims x 8 heads] += V^T P^T (V fragments by ldmatrix.trans). The
+//    GQA group of up to 8 query heads is the mma's N dimension, so each K/V
+//    byte is read once for the whole group. The softmax denominator sums the
+//    bf16-rounded weights that multiply V, so the output is an exact convex
+//    combination of V rows up to fp32 rounding.
+//  * Tokens past the context in the last block are masked: their scores are
+//    set to -inf and their V values to zero before the mma, so unwritten
+//    (even non-finite) slots never reach the output.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <mutex>
+#include <vector>
+
+#include "pkv_internal.h"
+#include "pkv_ptx.cuh"
+
+namespace pkv {
+namespace attn {
+
+constexpr int kTok = PKV_BLOCK_TOKENS;   // tokens per block
+constexpr int kDim = PKV_ATTN_HEAD_DIM;  // head dim
+constexpr int kMaxG = PKV_ATTN_MAX_GROUP;
+constexpr int kConsumerWarps = 4;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kThreads = kConsumers + 32;
+constexpr int kStages = 8;
+constexpr int kQSlots = 4;
+constexpr int kHalfBytes = kTok * 64 * 2;  // one 16 x 64 bf16 box
+constexpr int kBlockBytes = 2 * kHalfBytes;  // one K (or V) block of one KV head
+constexpr int kStageBytes = 2 * kBlockBytes;
+constexpr int kQBytes = kMaxG * kDim * 2;
+constexpr int kORow = 132;  // floats per head row of merge buffers and partials
+constexpr int kPartialFloats = kMaxG * kORow;
+
+constexpr int kOffStages = 0;
+constexpr int kOffQ = kOffStages + kStages * kStageBytes;
+constexpr int kOffO = kOffQ + kQSlots * kQBytes;
+constexpr int kOffM = kOffO + kConsumerWarps * kMaxG * kORow * 4;
+constexpr int kOffL = kOffM + kConsumerWarps * kMaxG * 4;
+constexpr int kOffBar = kOffL + kConsumerWarps * kMaxG * 4;
+constexpr int kNumBars = 2 * kStages + 2 * kQSlots;
+constexpr int kOffMisc = kOffBar + kNumBars * 8;
+constexpr int kOffScan = kOffMisc + 64;
+
+constexpr size_t smem_bytes(int num_seqs) { return 1024 + kOffScan + 4 * static_cast<size_t>(num_seqs); }
+
+constexpr size_t kWsHeader = 256;
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+inline size_t workspace_bytes(int num_seqs, int num_kv_heads, int grid) {
+    return kWsHeader + align256(static_cast<size_t>(num_seqs) * num_kv_heads * 4) +
+           static_cast<size_t>(grid) * 2 * kPartialFloats * 4;
+}
+
+struct Params {
+    const __nv_bfloat16* q;
+    __nv_bfloat16* out;
+    const int32_t* block_tables;
+    const int32_t* context_lens;
+    int num_seqs;
+    int num_q_heads;
+    int num_kv_heads;
+    int group;
+    int max_blocks;
+    int num_blocks;
+    float scale_log2;
+    uint32_t* err;
+    int* counters;
+    float* partials;
+};
+
+// Position in the line of (sequence, KV head) block runs.
+struct Cursor {
+    int s, g, blk;
+};
+
+__device__ __forceinline__ int run_blocks(const int* scan, int s) {
+    return scan[s] - (s > 0 ? scan[s - 1] : 0);
+}
+
+// Smallest s with scan[s] > t (scan is the inclusive prefix of run lengths).
+__device__ __forceinline__ int find_seq(const int* scan, int n, int t) {
+    int lo = 0, hi = n - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (scan[mid] > t) hi = mid; else lo = mid + 1;
+    }
+    return lo;
+}
+
+__device__ __forceinline__ Cursor locate(const int* scan, int n, int hkv, long long x) {
+    Cursor c;
+    c.s = find_seq(scan, n, static_cast<int>(x / hkv));
+    const int nb = run_blocks(scan, c.s);
+    const long long off = x - static_cast<long long>(hkv) * (scan[c.s] - nb);
+    c.g = static_cast<int>(off / nb);
+    c.blk = static_cast<int>(off % nb);
+    return c;
+}
+
+__device__ __forceinline__ void advance(Cursor& c, const int* scan, int n, int hkv, int len) {
+    c.blk += len;
+    if (c.blk == run_blocks(scan, c.s)) {
+        c.blk = 0;
+        if (++c.g == hkv) {
+            c.g = 0;
+            do { ++c.s; } while (c.s < n && run_blocks(scan, c.s) == 0);
+        }
+    }
+}
+
+__device__ __forceinline__ int clamped_ctx(const Params& p, int s) {
+    int c = __ldg(p.context_lens + s);
+    const int cap = p.max_blocks * kTok;
+    if (c > cap) c = cap;
+    return c;
+}
+
+__global__ void __launch_bounds__(kThreads, 2)
+decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+              const Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int B = p.num_seqs;
+    const int Hkv = p.num_kv_heads;
+    const int G = p.group;
+
+    int* scan = reinterpret_cast<int*>(smem + kOffScan);
+    int* misc = reinterpret_cast<int*>(smem + kOffMisc);
+    volatile int* abort_flag = misc;      // misc[0]
+    volatile int* merge_flag = misc + 1;  // misc[1]
+    int* warp_tot = misc + 8;             // misc[8 .. 8 + 5)
+    const uint32_t bar0 = smem_u32(smem + kOffBar);
+    auto full_bar = [&](int i) { return bar0 + 8u * i; };
+    auto empty_bar = [&](int i) { return bar0 + 8u * (kStages + i); };
+    auto qfull_bar = [&](int i) { return bar0 + 8u * (2 * kStages + i); };
+    auto qempty_bar = [&](int i) { return bar0 + 8u * (2 * kStages + kQSlots + i); };
+
+    if (tid == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(full_bar(i), 1);
+            mbar_init(empty_bar(i), 1);
+        }
+        for (int i = 0; i < kQSlots; ++i) {
+            mbar_init(qfull_bar(i), 1);
+            mbar_init(qempty_bar(i), kConsumerWarps);
+        }
+        misc[0] = 0;
+        misc[1] = 0;
+        fence_barrier_init();
+    }
+
+    // ---- plan: inclusive prefix sum of block-run lengths over sequences ----
+    {
+        const int per = (B + kThreads - 1) / kThreads;
+        const int lo = min(B, tid * per);
+        const int hi = min(B, lo + per);
+        const int cap = p.max_blocks * kTok;
+        int local = 0;
+        for (int s = lo; s < hi; ++s) {
+            const int c = __ldg(p.context_lens + s);
+            if (c > cap && p.err) atomicOr(p.err, PKV_DEVERR_CONTEXT);
+            const int cc = min(c, cap);
+            local += cc > 0 ? (cc + kTok - 1) / kTok : 0;
+        }
+        int v = local;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, v, off);
+            if (lane >= off) v += n;
+        }
+        if (lane == 31) warp_tot[warp] = v;
+        __syncthreads();
+        int run = v - local;
+        for (int w = 0; w < warp; ++w) run += warp_tot[w];
+        for (int s = lo; s < hi; ++s) {
+            const int cc = clamped_ctx(p, s);
+            run += cc > 0 ? (cc + kTok - 1) / kTok : 0;
+            scan[s] = run;
+        }
+        __syncthreads();
+    }
+
+    const long long total = static_cast<long long>(Hkv) * scan[B - 1];
+    const long long chunk = (total + gridDim.x - 1) / gridDim.x;
+    const long long range_lo = min(total, static_cast<long long>(blockIdx.x) * chunk);
+    const long long range_hi = min(total, range_lo + chunk);
+
+    // Sequences with no context get a zero output row (CTA 0, consumer warps).
+    if (blockIdx.x == 0 && warp < kConsumerWarps) {
+        const int row_vec = p.num_q_heads * kDim / 8;
+        for (int s = warp; s < B; s += kConsumerWarps) {
+            if (run_blocks(scan, s) != 0) continue;
+            uint4* dst = reinterpret_cast<uint4*>(p.out + static_cast<size_t>(s) * p.num_q_heads * kDim);
+            for (int i = lane; i < row_vec; i += 32) dst[i] = make_uint4(0, 0, 0, 0);
+        }
+    }
+    if (range_lo >= range_hi) return;
+
+    if (warp == kConsumerWarps) {
+        // ======================= producer warp =======================
+        const uint64_t policy = policy_evict_first();
+        if (lane == 0) {
+            prefetch_tensormap(&tm_k);
+            prefetch_tensormap(&tm_v);
+        }
+        Cursor cur = locate(scan, B, Hkv, range_lo);
+        long long x = range_lo;
+        int stage = 0, qslot = 0;
+        uint32_t sphase = 0, qphase = 0;
+        long long issued = 0;
+        int q_issued = 0;
+        while (x < range_hi) {
+            const int nb = run_blocks(scan, cur.s);
+            const int len = static_cast<int>(min(static_cast<long long>(nb - cur.blk), range_hi - x));
+            if (lane == 0) {
+                if (mbar_wait(qempty_bar(qslot), qphase ^ 1u, abort_flag, p.err)) {
+                    mbar_arrive_expect_tx(qfull_bar(qslot), G * kDim * 2);
+                    const __nv_bfloat16* src =
+                        p.q + (static_cast<size_t>(cur.s) * p.num_q_heads + static_cast<size_t>(cur.g) * G) * kDim;
+                    bulk_load(smem_u32(smem + kOffQ + qslot * kQBytes), src, G * kDim * 2, qfull_bar(qslot));
+                    ++q_issued;
+                }
+            }
+            if (++qslot == kQSlots) { qslot = 0; qphase ^= 1u; }
+            const int32_t* row = p.block_tables + static_cast<size_t>(cur.s) * p.max_blocks + cur.blk;
+            for (int j0 = 0; j0 < len; j0 += 32) {
+                int bid = 0;
+                if (j0 + lane < len) {
+                    bid = __ldg(row + j0 + lane);
+                    if (bid < 0 || bid >= p.num_blocks) {
+                        if (p.err) atomicOr(p.err, PKV_DEVERR_BLOCK_ID);
+                        bid = 0;  // read a valid block instead; the output is flagged invalid
+                    }
+                }
+                const int n = min(32, len - j0);
+                for (int jj = 0; jj < n; ++jj) {
+                    const int b = __shfl_sync(0xffffffffu, bid, jj);
+                    if (lane == 0) {
+                        if (mbar_wait(empty_bar(stage), sphase ^ 1u, abort_flag, p.err)) {
+                            const uint32_t fb = full_bar(stage);
+                            mbar_arrive_expect_tx(fb, kStageBytes);
+                            const int y = (b * Hkv + cur.g) * kTok;
+                            const uint32_t dst = smem_u32(smem + kOffStages + stage * kStageBytes);
+                            tma_load_2d(dst, &tm_k, 0, y, fb, policy);
+                            tma_load_2d(dst + kHalfBytes, &tm_k, 64, y, fb, policy);
+                            tma_load_2d(dst + kBlockBytes, &tm_v, 0, y, fb, policy);
+                            tma_load_2d(dst + kBlockBytes + kHalfBytes, &tm_v, 64, y, fb, policy);
+                            ++issued;
+                        }
+                    }
+                    if (++stage == kStages) { stage = 0; sphase ^= 1u; }
+                }
+            }
+            advance(cur, scan, B, Hkv, len);
+            x += len;
+        }
+        // If the pipeline was abandoned, wait (bounded) for the copies still in
+        // flight so that no TMA lands in shared memory after the CTA exits.
+        // Copies were issued in order up to the first failed wait, so the ones
+        // that can still be in flight are the last kStages blocks and the last
+        // kQSlots query loads issued.
+        if (lane == 0 && *abort_flag) {
+            volatile int never = 0;
+            for (long long i = max(0ll, issued - kStages); i < issued; ++i)
+                mbar_wait(full_bar(static_cast<int>(i % kStages)),
+                          static_cast<uint32_t>((i / kStages) & 1), &never, nullptr);
+            for (int i = max(0, q_issued - kQSlots); i < q_issued; ++i)
+                mbar_wait(qfull_bar(i % kQSlots), static_cast<uint32_t>((i / kQSlots) & 1), &never, nullptr);
+        }
+        return;
+    }
+
+    // ========================= consumer warps =========================
+    const int r = lane >> 2;  // mma group id: token row / head column owner
+    const int c = lane & 3;   // thread in group
+    float* sm_o = reinterpret_cast<float*>(smem + kOffO);
+    float* sm_m = reinterpret_cast<float*>(smem + kOffM);
+    float* sm_l = reinterpret_cast<float*>(smem + kOffL);
+    const uint32_t stage_base = smem_u32(smem + kOffStages);
+    // ldmatrix address pieces (row of the 16 x 16 tile each lane points at)
+    const uint32_t k_row_off = static_cast<uint32_t>(lane & 15) * 128u;
+    const int k_sw = lane & 7;
+    const int k_hi = lane >> 4;
+    const int v_mat = lane >> 3;
+    const uint32_t v_row_off = static_cast<uint32_t>((lane & 7) + ((v_mat >> 1) << 3)) * 128u;
+    const int v_sw = lane & 7;
+    const float NEG_INF = -INFINITY;
+
+    Cursor cur = locate(scan, B, Hkv, range_lo);
+    long long x = range_lo;
+    long long gidx0 = 0;
+    int qslot = 0;
+    uint32_t qphase = 0;
+    while (x < range_hi) {
+        const int s = cur.s, g = cur.g, blk0 = cur.blk;
+        const int nb = run_blocks(scan, s);
+        const int len = static_cast<int>(min(static_cast<long long>(nb - blk0), range_hi - x));
+        const int ctx = clamped_ctx(p, s);
+
+        // ---- query fragments (B operand of S^T = K Q^T) ----
+        uint32_t qb[16];
+        mbar_wait(qfull_bar(qslot), qphase, abort_flag, p.err);
+        {
+            const uint8_t* qs = smem + kOffQ + qslot * kQBytes + r * (kDim * 2) + c * 4;
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                qb[2 * ks] = r < G ? *reinterpret_cast<const uint32_t*>(qs + ks * 32) : 0u;
+                qb[2 * ks + 1] = r < G ? *reinterpret_cast<const uint32_t*>(qs + ks * 32 + 16) : 0u;
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(qempty_bar(qslot));
+        if (++qslot == kQSlots) { qslot = 0; qphase ^= 1u; }
+
+        float m0 = NEG_INF, m1 = NEG_INF, l0 = 0.f, l1 = 0.f;
+        float o[8][4];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+
+        for (int jb = warp; jb < len; jb += kConsumerWarps) {
+            const long long gi = gidx0 + jb;
+            const int st = static_cast<int>(gi % kStages);
+            mbar_wait(full_bar(st), static_cast<uint32_t>((gi / kStages) & 1), abort_flag, p.err);
+            const int valid = (blk0 + jb == nb - 1) ? ctx - kTok * (nb - 1) : kTok;
+            const uint32_t sk = stage_base + st * kStageBytes;
+            const uint32_t sv = sk + kBlockBytes;
+
+            // S^T = K Q^T : two accumulators halve the dependent mma chain.
+            float sa[4] = {0.f, 0.f, 0.f, 0.f};
+            float sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const int chunk = ((ks & 3) << 1) | k_hi;
+                uint32_t a[4];
+                ldmatrix_x4(a, sk + (ks >> 2) * kHalfBytes + k_row_off + ((chunk ^ k_sw) << 4));
+                if (ks & 1) mma_bf16_16816(sb, a, qb[2 * ks], qb[2 * ks + 1]);
+                else mma_bf16_16816(sa, a, qb[2 * ks], qb[2 * ks + 1]);
+            }
+            float x0 = (sa[0] + sb[0]) * p.scale_log2;  // token r,   head 2c
+            float x1 = (sa[1] + sb[1]) * p.scale_log2;  // token r,   head 2c+1
+            float x2 = (sa[2] + sb[2]) * p.scale_log2;  // token r+8, head 2c
+            float x3 = (sa[3] + sb[3]) * p.scale_log2;  // token r+8, head 2c+1
+            uint32_t vmask01 = 0xffffffffu, vmask23 = 0xffffffffu;
+            if (valid < kTok) {
+                if (r >= valid) x0 = x1 = NEG_INF;
+                if (r + 8 >= valid) x2 = x3 = NEG_INF;
+                vmask01 = (2 * c < valid ? 0x0000ffffu : 0u) | (2 * c + 1 < valid ? 0xffff0000u : 0u);
+                vmask23 = (2 * c + 8 < valid ? 0x0000ffffu : 0u) | (2 * c + 9 < valid ? 0xffff0000u : 0u);
+            }
+            float bm0 = fmaxf(x0, x2), bm1 = fmaxf(x1, x3);
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
+                bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
+            }
+            const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
+            const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);
+            m0 = mn0;
+            m1 = mn1;
+            const uint32_t p01 = pack_bf16x2(ex2(x0 - mn0), ex2(x1 - mn1));  // token r
+            const uint32_t p23 = pack_bf16x2(ex2(x2 - mn0), ex2(x3 - mn1));  // token r+8
+            l0 = l0 * al0 + bf16_lo(p01) + bf16_lo(p23);
+            l1 = l1 * al1 + bf16_hi(p01) + bf16_hi(p23);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                o[j][0] *= al0;
+                o[j][1] *= al1;
+                o[j][2] *= al0;
+                o[j][3] *= al1;
+            }
+            const uint32_t pb0 = movmatrix_trans(p01);  // P^T rows: tokens 2c, 2c+1; column: head r
+            const uint32_t pb1 = movmatrix_trans(p23);  // tokens 2c+8, 2c+9
+
+            // O^T += V^T P^T over the 8 16-dim tiles of the head.
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int chunk = ((j & 3) << 1) | (v_mat & 1);
+                uint32_t a[4];
+                ldmatrix_x4_trans(a, sv + (j >> 2) * kHalfBytes + v_row_off + ((chunk ^ v_sw) << 4));
+                a[0] &= vmask01;
+                a[1] &= vmask01;
+                a[2] &= vmask23;
+                a[3] &= vmask23;
+                mma_bf16_16816(o[j], a, pb0, pb1);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty_bar(st));
+        }
+        gidx0 += len;
+
+        // ---- merge the consumer warps' states for this piece ----
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+        }
+        if (r == 0) {
+            sm_m[warp * kMaxG + 2 * c] = m0;
+            sm_m[warp * kMaxG + 2 * c + 1] = m1;
+            sm_l[warp * kMaxG + 2 * c] = l0;
+            sm_l[warp * kMaxG + 2 * c + 1] = l1;
+        }
+        named_barrier_sync(1, kConsumers);
+        {
+            float M0 = NEG_INF, M1 = NEG_INF;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) {
+                M0 = fmaxf(M0, sm_m[w * kMaxG + 2 * c]);
+                M1 = fmaxf(M1, sm_m[w * kMaxG + 2 * c + 1]);
+            }
+            const float f0 = m0 == NEG_INF ? 0.f : ex2(m0 - M0);
+            const float f1 = m1 == NEG_INF ? 0.f : ex2(m1 - M1);
+            float* o0 = sm_o + (warp * kMaxG + 2 * c) * kORow + r;
+            float* o1 = o0 + kORow;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                o0[16 * j] = o[j][0] * f0;
+                o1[16 * j] = o[j][1] * f1;
+                o0[16 * j + 8] = o[j][2] * f0;
+                o1[16 * j + 8] = o[j][3] * f1;
+            }
+        }
+        named_barrier_sync(1, kConsumers);
+
+        const long long seg_start = static_cast<long long>(Hkv) * (scan[s] - nb) + static_cast<long long>(g) * nb;
+        const long long seg_end = seg_start + nb;
+        const int i0 = static_cast<int>(seg_start / chunk);
+        const int i1 = static_cast<int>((seg_end - 1) / chunk);
+        const int pieces = i1 - i0 + 1;
+        const int h = tid >> 4;
+        const int d0 = (tid & 15) * 8;
+        __nv_bfloat16* out_row = p.out + (static_cast<size_t>(s) * p.num_q_heads + static_cast<size_t>(g) * G + h) * kDim + d0;
+        if (h < G) {
+            float Mh = NEG_INF;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) Mh = fmaxf(Mh, sm_m[w * kMaxG + h]);
+            float Lh = 0.f;
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) {
+                const float mw = sm_m[w * kMaxG + h];
+                if (mw != NEG_INF) Lh += sm_l[w * kMaxG + h] * ex2(mw - Mh);
+                const float4* src = reinterpret_cast<const float4*>(sm_o + (w * kMaxG + h) * kORow + d0);
+                const float4 u = src[0], v = src[1];
+                acc[0] += u.x; acc[1] += u.y; acc[2] += u.z; acc[3] += u.w;
+                acc[4] += v.x; acc[5] += v.y; acc[6] += v.z; acc[7] += v.w;
+            }
+            if (pieces == 1) {
+                const float inv = 1.f / Lh;
+                uint4 w4;
+                w4.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+                w4.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+                w4.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
+                w4.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
+                *reinterpret_cast<uint4*>(out_row) = w4;
+            } else {
+                const int slot = (x == range_lo) ? 0 : 1;
+                float* part = p.partials + (static_cast<size_t>(blockIdx.x) * 2 + slot) * kPartialFloats + h * kORow;
+                reinterpret_cast<float4*>(part + d0)[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+                reinterpret_cast<float4*>(part + d0)[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+                if ((tid & 15) == 0) {
+                    part[kDim] = Mh;
+                    part[kDim + 1] = Lh;
+                }
+            }
+        }
+        if (pieces > 1) {
+            __threadfence();
+            named_barrier_sync(1, kConsumers);
+            if (tid == 0) {
+                const int old = atomicAdd(p.counters + s * Hkv + g, 1);
+                *merge_flag = (old == pieces - 1);
+            }
+            named_barrier_sync(1, kConsumers);
+            if (*merge_flag) {
+                __threadfence();
+                if (h < G) {
+                    const int slot0 = (seg_start == static_cast<long long>(i0) * chunk) ? 0 : 1;
+                    float Mx = NEG_INF;
+                    for (int i = i0; i <= i1; ++i) {
+                        const float* part = p.partials + (static_cast<size_t>(i) * 2 + (i == i0 ? slot0 : 0)) * kPartialFloats + h * kORow;
+                        Mx = fmaxf(Mx, __ldcg(part + kDim));
+                    }
+                    float L = 0.f;
+                    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                    for (int i = i0; i <= i1; ++i) {
+                        const float* part = p.partials + (static_cast<size_t>(i) * 2 + (i == i0 ? slot0 : 0)) * kPartialFloats + h * kORow;
+                        const float f = ex2(__ldcg(part + kDim) - Mx);
+                        L += f * __ldcg(part + kDim + 1);
+                        const float4 u = __ldcg(reinterpret_cast<const float4*>(part + d0));
+                        const float4 v = __ldcg(reinterpret_cast<const float4*>(part + d0) + 1);
+                        acc[0] += f * u.x; acc[1] += f * u.y; acc[2] += f * u.z; acc[3] += f * u.w;
+                        acc[4] += f * v.x; acc[5] += f * v.y; acc[6] += f * v.z; acc[7] += f * v.w;
+                    }
+                    const float inv = 1.f / L;
+                    uint4 w4;
+                    w4.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+                    w4.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+                    w4.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
+                    w4.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
+                    *reinterpret_cast<uint4*>(out_row) = w4;
+                }
+                if (tid == 0) p.counters[s * Hkv + g] = 0;  // ready for the next launch
+            }
+        }
+        named_barrier_sync(1, kConsumers);  // merge buffers are free again
+
+        advance(cur, scan, B, Hkv, len);
+        x += len;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+
+using EncodeTiledFn = PFN_cuTensorMapEncodeTiled_v12000;
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// 2-D view of a cache: rows = num_blocks * Hkv * 16 token rows of 128 bf16.
+bool make_cache_map(CUtensorMap* map, const void* base, int num_blocks, int hkv) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(kDim),
+                          static_cast<cuuint64_t>(num_blocks) * hkv * kTok};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(kDim) * 2};
+    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kTok)};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct DeviceInfo {
+    bool ok = false;
+    int sm_count = 0;
+    int ctas_per_sm = 0;
+    int grid = 0;
+};
+
+DeviceInfo device_info() {
+    static std::mutex mu;
+    static std::vector<DeviceInfo> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return {};
+    std::lock_guard<std::mutex> lock(mu);
+    if (static_cast<int>(cache.size()) <= dev) cache.resize(dev + 1);
+    DeviceInfo& d = cache[dev];
+    if (d.ok) return d;
+    const size_t smem_max = smem_bytes(PKV_ATTN_MAX_SEQS);
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem_max));
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.ctas_per_sm, decode_kernel, kThreads, smem_max);
+    if (e != cudaSuccess || d.ctas_per_sm < 1) {
+        record_cuda_error(e);
+        return {};
+    }
+    d.grid = d.sm_count * d.ctas_per_sm;
+    d.ok = true;
+    return d;
+}
+
+}  // namespace attn
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+int pkv_attn_default_ctas(void) {
+    const attn::DeviceInfo d = attn::device_info();
+    return d.ok ? d.grid : 0;
+}
+
+size_t pkv_attn_workspace_size(int num_seqs, int num_kv_heads) {
+    if (num_seqs <= 0 || num_kv_heads <= 0) return 0;
+    const attn::DeviceInfo d = attn::device_info();
+    if (!d.ok) return 0;
+    return attn::workspace_bytes(num_seqs, num_kv_heads, d.grid);
+}
+
+pkv_status pkv_attn_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
+    if (!workspace || workspace_bytes < attn::kWsHeader) return PKV_EINVAL;
+    const cudaError_t e = cudaMemsetAsync(workspace, 0, workspace_bytes, as_stream(stream));
+    if (e != cudaSuccess) {
+        record_cuda_error(e);
+        return PKV_ECUDA;
+    }
+    return PKV_OK;
+}
+
+pkv_status pkv_attn_decode(const void* q, const void* k_cache, const void* v_cache,
+                           const int32_t* block_tables, int max_blocks_per_seq,
+                           const int32_t* context_lens, int num_seqs, int num_q_heads,
+                           int num_kv_heads, int head_dim, int num_blocks, float scale,
+                           int num_ctas, void* workspace, size_t workspace_bytes, void* out,
+                           void* stream) {
+    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !workspace || !out)
+        return PKV_EINVAL;
+    if (num_seqs < 1 || num_q_heads < 1 || num_kv_heads < 1 || num_blocks < 1 ||
+        max_blocks_per_seq < 1 || num_ctas < 0 || !std::isfinite(scale))
+        return PKV_EINVAL;
+    if (num_seqs > PKV_ATTN_MAX_SEQS || head_dim != PKV_ATTN_HEAD_DIM ||
+        num_q_heads % num_kv_heads != 0 || num_q_heads / num_kv_heads > PKV_ATTN_MAX_GROUP)
+        return PKV_EUNSUPPORTED;
+    if (static_cast<long long>(num_blocks) * num_kv_heads * PKV_BLOCK_TOKENS >= (1ll << 31) ||
+        static_cast<long long>(num_seqs) * max_blocks_per_seq >= (1ll << 31) ||
+        static_cast<long long>(max_blocks_per_seq) * PKV_BLOCK_TOKENS >= (1ll << 31) ||
+        static_cast<long long>(num_kv_heads) * num_seqs * max_blocks_per_seq >= (1ll << 31))
+        return PKV_ERANGE;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return PKV_EINVAL;
+    const attn::DeviceInfo d = attn::device_info();
+    if (!d.ok) return PKV_ECUDA;
+    int grid = num_ctas > 0 ? num_ctas : d.grid;
+    const size_t fixed = attn::kWsHeader + attn::align256(static_cast<size_t>(num_seqs) * num_kv_heads * 4);
+    if (workspace_bytes < fixed + 2 * attn::kPartialFloats * 4) return PKV_EINVAL;
+    const long long fit = static_cast<long long>((workspace_bytes - fixed) / (2 * attn::kPartialFloats * 4));
+    if (grid > fit) {
+        if (num_ctas > 0) return PKV_EINVAL;
+        grid = static_cast<int>(fit);
+    }
+
+    CUtensorMap tm_k, tm_v;
+    if (!attn::make_cache_map(&tm_k, k_cache, num_blocks, num_kv_heads) ||
+        !attn::make_cache_map(&tm_v, v_cache, num_blocks, num_kv_heads))
+        return PKV_ECUDA;
+
+    attn::Params prm;
+    prm.q = static_cast<const __nv_bfloat16*>(q);
+    prm.out = static_cast<__nv_bfloat16*>(out);
+    prm.block_tables = block_tables;
+    prm.context_lens = context_lens;
+    prm.num_seqs = num_seqs;
+    prm.num_q_heads = num_q_heads;
+    prm.num_kv_heads = num_kv_heads;
+    prm.group = num_q_heads / num_kv_heads;
+    prm.max_blocks = max_blocks_per_seq;
+    prm.num_blocks = num_blocks;
+    prm.scale_log2 = scale * 1.4426950408889634f;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    prm.err = reinterpret_cast<uint32_t*>(ws);
+    prm.counters = reinterpret_cast<int*>(ws + attn::kWsHeader);
+    prm.partials = reinterpret_cast<float*>(ws + fixed);
+
+    attn::decode_kernel<<<grid, attn::kThreads, attn::smem_bytes(num_seqs), as_stream(stream)>>>(tm_k, tm_v, prm);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        record_cuda_error(e);
+        return PKV_ECUDA;
+    }
+    return PKV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,143 @@
+"""One attention layer's paged KV cache on one GPU.
+
+The pool is allocated once as two device arrays [num_blocks, Hkv, 16, D]
+("The inference server": the KV cache is one arena allocated at start-up,
+managed by block tables, with no allocator on the hot path). The C++ block
+manager owns the tables; a decode step is host bookkeeping (slots and
+copy-on-write pairs from pkv_bm_prepare_append, cs2680 Lecture 10, §10.5's
+"allocate blocks to grow") followed by three launches on one stream: block
+copy, append, attention.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+from . import _native as nat
+
+
+def bf16_from_bits(bits: np.ndarray) -> torch.Tensor:
+    """uint16 bf16 bit patterns -> CPU bf16 tensor sharing no arithmetic."""
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+
+
+def bits_from_bf16(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+@dataclass
+class StepBuffers:
+    """Device inputs and output of one decode step (shapes fixed per batch)."""
+    seq_ids: list
+    slots: torch.Tensor       # int64 [B]
+    pairs: torch.Tensor       # int32 [n, 2]
+    tables: torch.Tensor      # int32 [B, W]
+    ctx: torch.Tensor         # int32 [B]
+    q: torch.Tensor           # bf16 [B, Hq, D]
+    k: torch.Tensor           # bf16 [B, Hkv, D]
+    v: torch.Tensor           # bf16 [B, Hkv, D]
+    out: torch.Tensor         # bf16 [B, Hq, D]
+    workspace: nat.AttentionWorkspace
+
+    @property
+    def num_pairs(self) -> int:
+        return int(self.pairs.shape[0])
+
+
+class PagedKVEngine:
+    def __init__(self, num_blocks: int, num_q_heads: int, num_kv_heads: int, head_dim: int = 128,
+                 device="cuda", free_order=None):
+        self.num_blocks, self.num_q_heads, self.num_kv_heads, self.head_dim = (
+            num_blocks, num_q_heads, num_kv_heads, head_dim)
+        self.device = torch.device(device)
+        shape = (num_blocks, num_kv_heads, nat.BLOCK_TOKENS, head_dim)
+        self.k_cache = torch.empty(shape, dtype=torch.bfloat16, device=self.device)
+        self.v_cache = torch.empty(shape, dtype=torch.bfloat16, device=self.device)
+        self.bm = nat.BlockManager(num_blocks, nat.BLOCK_TOKENS, free_order)
+        self.error = nat.new_error_word(self.device)
+
+    # ---- pool content ----------------------------------------------------
+    def load_pool(self, k_bits: np.ndarray, v_bits: np.ndarray, lo: int = 0) -> None:
+        n = k_bits.shape[0]
+        self.k_cache[lo : lo + n].copy_(bf16_from_bits(k_bits))
+        self.v_cache[lo : lo + n].copy_(bf16_from_bits(v_bits))
+
+    def load_workload_pool(self, w, chunk_blocks: int = 4096) -> None:
+        for lo in range(0, w.pool_blocks, chunk_blocks):
+            hi = min(w.pool_blocks, lo + chunk_blocks)
+            self.load_pool(w.pool_blocks_range("k", lo, hi), w.pool_blocks_range("v", lo, hi), lo)
+
+    # ---- host bookkeeping + device launches ---------------------------------
+    def append_tokens(self, seq_ids, k: torch.Tensor, v: torch.Tensor, stream=None):
+        """Append one token per sequence (k, v: [B, Hkv, D] bf16 on device);
+        returns (slots, pairs) as the block manager decided them."""
+        slots, pairs = self.bm.prepare_append(list(seq_ids))
+        if pairs:
+            pt = torch.tensor(pairs, dtype=torch.int32).to(self.device, non_blocking=True)
+            nat.block_copy(self.k_cache, self.v_cache, pt, self.error, stream)
+        st = torch.tensor(slots, dtype=torch.int64).to(self.device, non_blocking=True)
+        nat.append(k, v, st, self.k_cache, self.v_cache, self.error, stream)
+        return slots, pairs
+
+    def replay_events(self, w, with_content: bool = True):
+        """Apply a workload's admit / fork / history events; history appends
+        write the workload's history K/V when with_content is set."""
+        history = []
+        for ei, ev in enumerate(w.events):
+            if ev[0] == "admit":
+                self.bm.admit(ev[1], ev[2], ev[3], ev[4])
+            elif ev[0] == "fork":
+                self.bm.fork(ev[1], ev[2])
+            elif ev[0] == "history":
+                counts = ev[1]
+                ids = sorted(counts)
+                for t in range(max(counts.values()) if counts else 0):
+                    batch = [s for s in ids if counts[s] > t]
+                    if with_content:
+                        kb, vb = w.history_inputs(ei, t, len(batch))
+                        k = bf16_from_bits(kb).to(self.device)
+                        v = bf16_from_bits(vb).to(self.device)
+                        slots, pairs = self.append_tokens(batch, k, v)
+                    else:
+                        slots, pairs = self.bm.prepare_append(batch)
+                    history.append((batch, slots, pairs))
+            else:
+                raise ValueError(f"unknown event {ev[0]}")
+        return history
+
+    def prepare_step(self, seq_ids, q_bits, k_bits, v_bits, width: int | None = None) -> StepBuffers:
+        """Host bookkeeping of one decode step (each sequence appends one
+        token) and its device inputs; the step itself is run_step."""
+        seq_ids = list(seq_ids)
+        slots, pairs = self.bm.prepare_append(seq_ids)
+        if width is None:
+            width = max(len(self.bm.table(s)) for s in seq_ids)
+        tables, ctx = self.bm.batch_tables(seq_ids, width)
+        dev = self.device
+        q = bf16_from_bits(q_bits).to(dev)
+        return StepBuffers(
+            seq_ids=seq_ids,
+            slots=torch.tensor(slots, dtype=torch.int64).to(dev),
+            pairs=torch.tensor(pairs, dtype=torch.int32).reshape(-1, 2).to(dev),
+            tables=tables.to(dev), ctx=ctx.to(dev), q=q,
+            k=bf16_from_bits(k_bits).to(dev), v=bf16_from_bits(v_bits).to(dev),
+            out=torch.empty_like(q),
+            workspace=nat.AttentionWorkspace(len(seq_ids), self.num_kv_heads, device=dev))
+
+    def run_step(self, sb: StepBuffers, scale: float, num_ctas: int = 0, stream=None) -> torch.Tensor:
+        """The device part of a decode step: copy-on-write copies, append,
+        attention. Idempotent for fixed inputs."""
+        if sb.num_pairs:
+            nat.block_copy(self.k_cache, self.v_cache, sb.pairs, self.error, stream)
+        nat.append(sb.k, sb.v, sb.slots, self.k_cache, self.v_cache, self.error, stream)
+        nat.attn_decode(sb.q, self.k_cache, self.v_cache, sb.tables, sb.ctx, scale, sb.out,
+                        sb.workspace, num_ctas, stream)
+        return sb.out
+
+    def read_errors(self, sb: StepBuffers | None = None) -> int:
+        e = nat.read_device_error(self.error)
+        if sb is not None:
+            e |= sb.workspace.read_error()
+        return e

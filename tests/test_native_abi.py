@@ -1,0 +1,60 @@
+"""The C-ABI library loads and exports every function include/pkv.h declares
+(no compute calls: these run without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib_path():
+    from paged_kv_cache_49_gb300 import build
+    return build.build()
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "pkv.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkv_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for required in ("pkv_append", "pkv_attn_decode", "pkv_block_copy", "pkv_bm_admit",
+                     "pkv_bm_prepare_append", "pkv_bm_free"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib_path):
+    lib = ctypes.CDLL(lib_path)
+    missing = [n for n in _declared() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_binding_covers_the_header(lib_path):
+    import paged_kv_cache_49_gb300 as pkv
+    assert sorted(pkv.EXPORTED) == _declared()
+
+
+def test_version_and_status_strings(lib_path):
+    import paged_kv_cache_49_gb300._native as nat
+    assert nat.lib.pkv_version() == 100
+    assert nat.lib.pkv_status_string(nat.PKV_ENOMEM) == b"too few free pages"
+    assert nat.lib.pkv_status_string(12345) == b"unknown status"
+
+
+def test_host_argument_checks_need_no_gpu(lib_path):
+    import paged_kv_cache_49_gb300._native as nat
+    L = nat.lib
+    # null pointers and bad shapes are rejected before any CUDA call
+    assert L.pkv_attn_decode(None, None, None, None, 1, None, 1, 32, 8, 128, 1, 1.0, 0, None, 0, None, None) == nat.PKV_EINVAL
+    assert L.pkv_append(None, None, None, -1, None, None, 1, 8, 128, None, None) == nat.PKV_EINVAL
+    assert L.pkv_append(None, None, None, 0, None, None, 1, 8, 128, None, None) == nat.PKV_OK
+    assert L.pkv_block_copy(None, None, None, 0, 1, 8, 128, None, None) == nat.PKV_OK
+    assert L.pkv_block_copy(None, None, None, 3, 1, 8, 127, None, None) == nat.PKV_EINVAL
+    assert L.pkv_attn_workspace_size(0, 8) == 0
+    assert L.pkv_bm_create(0, 16, None) is None
+    assert L.pkv_bm_create(4, 8, None) is None

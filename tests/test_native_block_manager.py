@@ -1,0 +1,156 @@
+"""The C++ block manager against the oracle's: the pages' worked numbers and
+bit-exact agreement (block ids, slots, copy pairs, refcounts, errors) over
+random operation sequences and the synthetic workloads' events. CPU only."""
+import random
+import threading
+
+import pytest
+
+from oracle import block_manager as obm
+from workloads import make_workload
+
+
+@pytest.fixture(scope="module")
+def nat():
+    from paged_kv_cache_49_gb300 import build
+    build.build()
+    import paged_kv_cache_49_gb300._native as n
+    return n
+
+
+def test_worked_admission_numbers(nat, golden):
+    g = golden["admission_32L"]
+    bm = nat.BlockManager(g["pool_pages"])
+    for _ in range(7):
+        bm.admit(g["prompt_tokens"], g["output_tokens"], 0, g["prompt_tokens"])
+    st = bm.stats()
+    assert st["used"] == g["seven_shared_pages"] and st["free"] == g["seven_shared_free_after"]
+    with pytest.raises(nat.PoolExhausted):
+        bm.admit(g["prompt_tokens"], g["output_tokens"], 0, g["prompt_tokens"])
+    assert bm.stats() == st
+    iso = nat.BlockManager(g["pool_pages"])
+    iso.admit(g["prompt_tokens"], g["output_tokens"], 0, g["prompt_tokens"])
+    assert iso.stats()["used"] == g["request_pages"]
+    with pytest.raises(nat.PoolExhausted):
+        iso.admit(g["prompt_tokens"], g["output_tokens"], 1, g["prompt_tokens"])
+
+
+def test_fanout_numbers(nat, golden):
+    g = golden["fanout_n8"]
+    bm = nat.BlockManager(4096)
+    p = bm.admit(g["prompt_tokens"], g["output_tokens"])
+    bm.fork(p, g["samples"] - 1)
+    assert bm.stats()["used"] * 16 == g["shared_tokens"]
+
+
+def _err_kind(nat, e):
+    if isinstance(e, (nat.PoolExhausted, obm.PoolExhausted)):
+        return "nomem"
+    if isinstance(e, (nat.ReservationExceeded, obm.ReservationExceeded)):
+        return "nospc"
+    return "inval"
+
+
+def _both(nat, fa, fb):
+    ra = rb = ea = eb = None
+    try:
+        ra = fa()
+    except (obm.BlockManagerError,) as e:
+        ea = _err_kind(nat, e)
+    try:
+        rb = fb()
+    except nat.PkvError as e:
+        eb = _err_kind(nat, e)
+    assert ea == eb
+    assert ra == rb
+    return ra
+
+
+def _same_state(o, n, ids):
+    assert o.stats() == n.stats()
+    for s in ids:
+        assert o.table(s) == n.table(s)
+        assert o.context_len(s) == n.context_len(s)
+    for b in range(o.num_blocks):
+        assert o.ref[b] == n.refcount(b)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_operations_match_oracle(nat, seed):
+    rnd = random.Random(seed)
+    nb = rnd.randint(16, 160)
+    order = rnd.sample(range(nb), nb) if seed % 2 else None
+    o = obm.BlockManager(nb, 16, order)
+    n = nat.BlockManager(nb, 16, order)
+    for _ in range(250):
+        live = sorted(o.seqs)
+        op = rnd.random()
+        if op < 0.3 or not live:
+            grp = rnd.choice([-1, -1, 0, 1])
+            p = rnd.randint(0, 60)
+            args = (p, rnd.randint(0, 40), grp, 16 * rnd.randint(0, p // 16) if grp >= 0 else 0)
+            _both(nat, lambda: o.admit(*args), lambda: n.admit(*args))
+        elif op < 0.45:
+            par, k = rnd.choice(live), rnd.randint(0, 3)
+            _both(nat, lambda: o.fork(par, k), lambda: n.fork(par, k))
+        elif op < 0.85:
+            ids = rnd.sample(live, rnd.randint(1, len(live)))
+            _both(nat, lambda: o.prepare_append(ids), lambda: n.prepare_append(ids))
+        elif op < 0.95:
+            s = rnd.choice(live)
+            _both(nat, lambda: o.free(s), lambda: n.free(s))
+        else:  # invalid calls
+            _both(nat, lambda: o.free(10 ** 6), lambda: n.free(10 ** 6))
+            if live:
+                _both(nat, lambda: o.prepare_append([live[0], live[0]]),
+                      lambda: n.prepare_append([live[0], live[0]]))
+        _same_state(o, n, sorted(o.seqs))
+
+
+@pytest.mark.parametrize("name", ["tiny", "tiny_nan", "prefix_admission", "fanout", "llama3_8b_b64"])
+def test_workload_events_match_oracle(nat, name):
+    w = make_workload(name)
+    o = obm.BlockManager(w.pool_blocks, 16, w.free_order)
+    n = nat.BlockManager(w.pool_blocks, 16, w.free_order)
+    for ev in w.events:
+        if ev[0] == "admit":
+            _both(nat, lambda: o.admit(*ev[1:]), lambda: n.admit(*ev[1:]))
+        elif ev[0] == "fork":
+            _both(nat, lambda: o.fork(ev[1], ev[2]), lambda: n.fork(ev[1], ev[2]))
+        else:
+            counts = ev[1]
+            ids = sorted(counts)
+            for t in range(max(counts.values()) if counts else 0):
+                batch = [s for s in ids if counts[s] > t]
+                _both(nat, lambda: o.prepare_append(batch), lambda: n.prepare_append(batch))
+    _both(nat, lambda: o.prepare_append(w.batch), lambda: n.prepare_append(w.batch))
+    _same_state(o, n, w.batch)
+    width = max(len(o.table(s)) for s in w.batch)
+    tables, ctx = n.batch_tables(w.batch, width)
+    for i, s in enumerate(w.batch):
+        t = o.table(s)
+        assert tables[i, : len(t)].tolist() == t and (tables[i, len(t):] == -1).all()
+        assert int(ctx[i]) == o.context_len(s)
+
+
+def test_concurrent_admissions_never_overcommit(nat):
+    # "Reserve the page a request has not written yet": two admissions that
+    # read the same free count must not both succeed past the pool.
+    bm = nat.BlockManager(256)
+    admitted, lock = [], threading.Lock()
+
+    def worker():
+        for _ in range(20):
+            try:
+                sid = bm.admit(2048, 257)
+                with lock:
+                    admitted.append(sid)
+            except nat.PoolExhausted:
+                pass
+
+    threads = [threading.Thread(target=worker) for _ in range(8)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert len(admitted) == 1 and bm.stats()["used"] == 145
