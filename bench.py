@@ -228,9 +228,9 @@ def run_ours(args):
     torch.cuda.set_device(local)
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    from paged_kv_cache_49_gb300 import build
     if rank == 0 or world == 1:
-        build.build()
+        from __graft_entry__ import _build_module
+        _build_module().build()
     if world > 1:
         dist.barrier()
     import paged_kv_cache_49_gb300 as pkv

@@ -18,3 +18,14 @@ def golden():
 
     with open(os.path.join(ROOT, "tests", "golden", "worked_numbers.json")) as f:
         return json.load(f)
+
+
+def build_native():
+    """Build libpkv.so if stale, without importing the package first."""
+    import importlib.util
+
+    path = os.path.join(ROOT, "paged_kv_cache_49_gb300", "build.py")
+    spec = importlib.util.spec_from_file_location("pkv_build", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod.build()

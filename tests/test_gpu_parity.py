@@ -20,8 +20,8 @@ MAX_ABS, MEAN_ABS = 2e-2, 2e-3
 @pytest.fixture(scope="module")
 def pkv():
     assert torch.cuda.is_available(), "GPU tests need a CUDA device"
-    from paged_kv_cache_49_gb300 import build
-    build.build()
+    from tests.conftest import build_native
+    build_native()
     import paged_kv_cache_49_gb300 as m
     return m
 

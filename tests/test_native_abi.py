@@ -11,8 +11,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def lib_path():
-    from paged_kv_cache_49_gb300 import build
-    return build.build()
+    from tests.conftest import build_native
+    return build_native()
 
 
 def _declared():

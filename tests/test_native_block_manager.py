@@ -12,8 +12,8 @@ from workloads import make_workload
 
 @pytest.fixture(scope="module")
 def nat():
-    from paged_kv_cache_49_gb300 import build
-    build.build()
+    from tests.conftest import build_native
+    build_native()
     import paged_kv_cache_49_gb300._native as n
     return n
 
