@@ -171,6 +171,36 @@ pkv_status pkv_attn_decode(const void* q, const void* k_cache, const void* v_cac
 /* Number of persistent CTAs pkv_attn_decode launches when num_ctas == 0. */
 int pkv_attn_default_ctas(void);
 
+/*
+ * pkv_attn_decode_static -- pkv_attn_decode without a workspace argument, for
+ * callers that cannot allocate device memory themselves (for example a plugin
+ * inside a host program that owns every device allocation and offers no
+ * allocator, or a latency-critical loop that must never call cudaMalloc or
+ * cudaFree). The pages describe no such variant: it has no counterpart there.
+ *
+ * Same computation, layouts and limits as pkv_attn_decode, plus:
+ *  - num_seqs * num_kv_heads <= 16384 (else PKV_ERANGE); at most 512
+ *    persistent CTAs;
+ *  - the scratch (counters and fp32 partials, about 4.2 MiB) is one static
+ *    device array inside this library; every GPU that loads the library holds
+ *    it until the process exits. This call allocates and frees nothing: it
+ *    clears the counters it uses with an asynchronous memset on `stream`,
+ *    then launches the kernel;
+ *  - the first call on a device looks up that array's device address (a
+ *    one-time set-up per device, with the device current); make that first
+ *    call before any stream capture;
+ *  - all calls share the one array, so calls that can overlap on the GPU
+ *    (different streams, or other host threads) race and give wrong results:
+ *    order them on one stream;
+ *  - device-side errors are ORed into *device_error when it is non-NULL
+ *    (a caller-owned device uint32); with NULL they are not reported.
+ */
+pkv_status pkv_attn_decode_static(const void* q, const void* k_cache, const void* v_cache,
+                                  const int32_t* block_tables, int max_blocks_per_seq,
+                                  const int32_t* context_lens, int num_seqs, int num_q_heads,
+                                  int num_kv_heads, int head_dim, int num_blocks, float scale,
+                                  uint32_t* device_error, void* out, void* stream);
+
 /* ---------------------------------------------------------------------------
  * Host block manager.
  *

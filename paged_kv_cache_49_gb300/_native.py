@@ -38,7 +38,7 @@ EXPORTED = [
     "pkv_attn_decode", "pkv_attn_default_ctas", "pkv_bm_create", "pkv_bm_destroy",
     "pkv_bm_admit", "pkv_bm_fork", "pkv_bm_prepare_append", "pkv_bm_free",
     "pkv_bm_block_table", "pkv_bm_context_len", "pkv_bm_batch_tables", "pkv_bm_stats",
-    "pkv_bm_refcount",
+    "pkv_bm_refcount", "pkv_attn_decode_static",
 ]
 
 
@@ -87,6 +87,7 @@ def _load() -> ctypes.CDLL:
         "pkv_attn_workspace_init": (i32, [vp, sz, vp]),
         "pkv_attn_decode": (i32, [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, f32, i32, vp, sz, vp, vp]),
         "pkv_attn_default_ctas": (i32, []),
+        "pkv_attn_decode_static": (i32, [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, f32, vp, vp, vp]),
         "pkv_bm_create": (vp, [i32, i32, vp]),
         "pkv_bm_destroy": (None, [vp]),
         "pkv_bm_admit": (i32, [vp, i32, i32, i32, i32, vp]),
@@ -241,6 +242,30 @@ def attn_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out=None
                                 block_tables.shape[1], _ptr(context_lens), B, hq, hkv, d, nb,
                                 float(scale), int(num_ctas), workspace.ptr, workspace.nbytes,
                                 _ptr(out), _stream(stream)), "pkv_attn_decode")
+    return out
+
+
+def attn_decode_static(q, k_cache, v_cache, block_tables, context_lens, scale, out, device_error=None,
+                       stream=None):
+    """attn_decode without a workspace, for callers that cannot allocate:
+    the library's own static device scratch is used and nothing is allocated
+    (out must be given). Calls on one device must not overlap on the GPU."""
+    _need(q, torch.bfloat16, "q")
+    _need(k_cache, torch.bfloat16, "k_cache")
+    _need(v_cache, torch.bfloat16, "v_cache")
+    _need(block_tables, torch.int32, "block_tables")
+    _need(context_lens, torch.int32, "context_lens")
+    _need(out, torch.bfloat16, "out")
+    B, hq, d = q.shape
+    nb, hkv, bt, d2 = k_cache.shape
+    if d != d2 or v_cache.shape != k_cache.shape or bt != BLOCK_TOKENS or out.shape != q.shape:
+        raise ValueError("q/out [B, Hq, D] and caches [NB, Hkv, 16, D] must agree")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or context_lens.shape != (B,):
+        raise ValueError("block_tables must be [B, W] and context_lens [B]")
+    _check(_lib.pkv_attn_decode_static(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                       block_tables.shape[1], _ptr(context_lens), B, hq, hkv, d, nb,
+                                       float(scale), _ptr(device_error), _ptr(out), _stream(stream)),
+           "pkv_attn_decode_static")
     return out
 
 

@@ -706,3 +706,118 @@ pkv_status pkv_attn_decode(const void* q, const void* k_cache, const void* v_cac
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of pkv_attn_decode.
+//
+// For callers that cannot allocate device memory themselves -- for example a
+// plugin loaded into a host program that owns every device allocation and
+// gives plugins no allocator, or a latency-critical loop that must never pay
+// for cudaMalloc / cudaFree. Instead of a caller-provided workspace, the
+// partial results and per-(sequence, KV head) counters live in one
+// file-scope device array that every GPU loading this library holds until
+// the process exits.
+
+namespace pkv {
+namespace attn {
+
+constexpr int kStaticMaxCtas = 512;       // partial slots: 2 per CTA
+constexpr int kStaticMaxPairs = 16384;    // num_seqs * num_kv_heads counters
+constexpr size_t kStaticCounterBytes = static_cast<size_t>(kStaticMaxPairs) * 4;
+constexpr size_t kStaticScratchBytes =
+    kWsHeader + kStaticCounterBytes + static_cast<size_t>(kStaticMaxCtas) * 2 * kPartialFloats * 4;
+
+static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+
+// Device address of g_static_scratch for the current device, looked up once
+// per device (the host-side name of the array is only a stand-in).
+uint8_t* static_scratch_address() {
+    static std::mutex mu;
+    static std::vector<uint8_t*> addr;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        record_cuda_error(e);
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (static_cast<int>(addr.size()) <= dev) addr.resize(dev + 1, nullptr);
+    if (!addr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_static_scratch);
+        if (e != cudaSuccess) {
+            record_cuda_error(e);
+            return nullptr;
+        }
+        addr[dev] = static_cast<uint8_t*>(p);
+    }
+    return addr[dev];
+}
+
+}  // namespace attn
+}  // namespace pkv
+
+extern "C" pkv_status pkv_attn_decode_static(const void* q, const void* k_cache, const void* v_cache,
+                                             const int32_t* block_tables, int max_blocks_per_seq,
+                                             const int32_t* context_lens, int num_seqs, int num_q_heads,
+                                             int num_kv_heads, int head_dim, int num_blocks, float scale,
+                                             uint32_t* device_error, void* out, void* stream) {
+    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return PKV_EINVAL;
+    if (num_seqs < 1 || num_q_heads < 1 || num_kv_heads < 1 || num_blocks < 1 || max_blocks_per_seq < 1 ||
+        !std::isfinite(scale))
+        return PKV_EINVAL;
+    if (num_seqs > PKV_ATTN_MAX_SEQS || head_dim != PKV_ATTN_HEAD_DIM || num_q_heads % num_kv_heads != 0 ||
+        num_q_heads / num_kv_heads > PKV_ATTN_MAX_GROUP)
+        return PKV_EUNSUPPORTED;
+    if (static_cast<long long>(num_seqs) * num_kv_heads > attn::kStaticMaxPairs) return PKV_ERANGE;
+    if (static_cast<long long>(num_blocks) * num_kv_heads * PKV_BLOCK_TOKENS >= (1ll << 31) ||
+        static_cast<long long>(num_seqs) * max_blocks_per_seq >= (1ll << 31) ||
+        static_cast<long long>(max_blocks_per_seq) * PKV_BLOCK_TOKENS >= (1ll << 31) ||
+        static_cast<long long>(num_kv_heads) * num_seqs * max_blocks_per_seq >= (1ll << 31))
+        return PKV_ERANGE;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return PKV_EINVAL;
+    const attn::DeviceInfo d = attn::device_info();
+    if (!d.ok) return PKV_ECUDA;
+    uint8_t* scratch = attn::static_scratch_address();
+    if (!scratch) return PKV_ECUDA;
+    const int grid = d.grid < attn::kStaticMaxCtas ? d.grid : attn::kStaticMaxCtas;
+
+    CUtensorMap tm_k, tm_v;
+    if (!attn::make_cache_map(&tm_k, k_cache, num_blocks, num_kv_heads) ||
+        !attn::make_cache_map(&tm_v, v_cache, num_blocks, num_kv_heads))
+        return PKV_ECUDA;
+
+    // The counters must start at zero; a previous call leaves them at zero
+    // unless it was cut short, so clear them (and the internal error word).
+    cudaError_t e = cudaMemsetAsync(scratch, 0,
+                                    attn::kWsHeader + static_cast<size_t>(num_seqs) * num_kv_heads * 4,
+                                    as_stream(stream));
+    if (e != cudaSuccess) {
+        record_cuda_error(e);
+        return PKV_ECUDA;
+    }
+
+    attn::Params prm;
+    prm.q = static_cast<const __nv_bfloat16*>(q);
+    prm.out = static_cast<__nv_bfloat16*>(out);
+    prm.block_tables = block_tables;
+    prm.context_lens = context_lens;
+    prm.num_seqs = num_seqs;
+    prm.num_q_heads = num_q_heads;
+    prm.num_kv_heads = num_kv_heads;
+    prm.group = num_q_heads / num_kv_heads;
+    prm.max_blocks = max_blocks_per_seq;
+    prm.num_blocks = num_blocks;
+    prm.scale_log2 = scale * 1.4426950408889634f;
+    prm.err = device_error ? device_error : reinterpret_cast<uint32_t*>(scratch);
+    prm.counters = reinterpret_cast<int*>(scratch + attn::kWsHeader);
+    prm.partials = reinterpret_cast<float*>(scratch + attn::kWsHeader + attn::kStaticCounterBytes);
+
+    attn::decode_kernel<<<grid, attn::kThreads, attn::smem_bytes(num_seqs), as_stream(stream)>>>(tm_k, tm_v, prm);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        record_cuda_error(e);
+        return PKV_ECUDA;
+    }
+    return PKV_OK;
+}
