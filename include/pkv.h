@@ -168,6 +168,30 @@ pkv_status pkv_attn_decode(const void* q, const void* k_cache, const void* v_cac
                            int num_ctas, void* workspace, size_t workspace_bytes,
                            void* out, void* stream);
 
+/*
+ * pkv_decode_step -- one decode step of one attention layer in one call:
+ * pkv_block_copy(src_dst_pairs), then pkv_append(k_new, v_new,
+ * slot_mapping), then pkv_attn_decode, on `stream`. "The inference server":
+ * the decode step is schedule, copy the block tables and lengths into the
+ * step's buffers, run -- with fixed-shape arguments. The arguments mean what
+ * they mean in the three calls (slot_mapping and src_dst_pairs come from
+ * pkv_bm_prepare_append); num_pairs or num_new_tokens may be 0.
+ * All arguments are checked before anything is launched. The attention
+ * kernel is launched so that its prologue (reading context_lens and
+ * block_tables, planning its split) overlaps the append; it waits for the
+ * append before reading the cache. Hence context_lens, block_tables and q
+ * must not be written by the copy or append of the same step (they are not,
+ * by construction). device_error receives copy and append errors; attention
+ * errors go to the workspace's error word as in pkv_attn_decode.
+ */
+pkv_status pkv_decode_step(const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                           int num_new_tokens, const int32_t* src_dst_pairs, int num_pairs,
+                           void* k_cache, void* v_cache, int num_blocks, const void* q,
+                           const int32_t* block_tables, int max_blocks_per_seq,
+                           const int32_t* context_lens, int num_seqs, int num_q_heads,
+                           int num_kv_heads, int head_dim, float scale, int num_ctas, void* workspace,
+                           size_t workspace_bytes, void* out, uint32_t* device_error, void* stream);
+
 /* Number of persistent CTAs pkv_attn_decode launches when num_ctas == 0. */
 int pkv_attn_default_ctas(void);
 

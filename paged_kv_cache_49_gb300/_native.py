@@ -38,7 +38,7 @@ EXPORTED = [
     "pkv_attn_decode", "pkv_attn_default_ctas", "pkv_bm_create", "pkv_bm_destroy",
     "pkv_bm_admit", "pkv_bm_fork", "pkv_bm_prepare_append", "pkv_bm_free",
     "pkv_bm_block_table", "pkv_bm_context_len", "pkv_bm_batch_tables", "pkv_bm_stats",
-    "pkv_bm_refcount", "pkv_attn_decode_static",
+    "pkv_bm_refcount", "pkv_attn_decode_static", "pkv_decode_step",
 ]
 
 
@@ -88,6 +88,8 @@ def _load() -> ctypes.CDLL:
         "pkv_attn_decode": (i32, [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, f32, i32, vp, sz, vp, vp]),
         "pkv_attn_default_ctas": (i32, []),
         "pkv_attn_decode_static": (i32, [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, f32, vp, vp, vp]),
+        "pkv_decode_step": (i32, [vp, vp, vp, i32, vp, i32, vp, vp, i32, vp, vp, i32, vp, i32, i32, i32, i32,
+                                  f32, i32, vp, sz, vp, vp, vp]),
         "pkv_bm_create": (vp, [i32, i32, vp]),
         "pkv_bm_destroy": (None, [vp]),
         "pkv_bm_admit": (i32, [vp, i32, i32, i32, i32, vp]),
@@ -242,6 +244,34 @@ def attn_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out=None
                                 block_tables.shape[1], _ptr(context_lens), B, hq, hkv, d, nb,
                                 float(scale), int(num_ctas), workspace.ptr, workspace.nbytes,
                                 _ptr(out), _stream(stream)), "pkv_attn_decode")
+    return out
+
+
+def decode_step(q, k_new, v_new, slot_mapping, pairs, k_cache, v_cache, block_tables, context_lens, scale,
+                out, workspace, device_error=None, num_ctas: int = 0, stream=None):
+    """One decode step in one library call: block copies (pairs [n, 2]),
+    append of k_new / v_new [B, Hkv, D] at slot_mapping, attention -> out."""
+    for t, dt, name in ((q, torch.bfloat16, "q"), (k_new, torch.bfloat16, "k_new"),
+                        (v_new, torch.bfloat16, "v_new"), (slot_mapping, torch.int64, "slot_mapping"),
+                        (pairs, torch.int32, "pairs"), (k_cache, torch.bfloat16, "k_cache"),
+                        (v_cache, torch.bfloat16, "v_cache"), (block_tables, torch.int32, "block_tables"),
+                        (context_lens, torch.int32, "context_lens"), (out, torch.bfloat16, "out")):
+        _need(t, dt, name)
+    B, hq, d = q.shape
+    nb, hkv, bt, d2 = k_cache.shape
+    T = slot_mapping.numel()
+    n = pairs.shape[0] if pairs.numel() else 0
+    if d != d2 or v_cache.shape != k_cache.shape or bt != BLOCK_TOKENS or out.shape != q.shape:
+        raise ValueError("q/out [B, Hq, D] and caches [NB, Hkv, 16, D] must agree")
+    if k_new.shape != (T, hkv, d) or v_new.shape != (T, hkv, d) or (n and pairs.shape != (n, 2)):
+        raise ValueError("k_new, v_new must be [T, Hkv, D]; pairs [n, 2]")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or context_lens.shape != (B,):
+        raise ValueError("block_tables must be [B, W] and context_lens [B]")
+    _check(_lib.pkv_decode_step(_ptr(k_new), _ptr(v_new), _ptr(slot_mapping), T, _ptr(pairs) if n else None, n,
+                                _ptr(k_cache), _ptr(v_cache), nb, _ptr(q), _ptr(block_tables),
+                                block_tables.shape[1], _ptr(context_lens), B, hq, hkv, d, float(scale),
+                                int(num_ctas), workspace.ptr, workspace.nbytes, _ptr(out), _ptr(device_error),
+                                _stream(stream)), "pkv_decode_step")
     return out
 
 

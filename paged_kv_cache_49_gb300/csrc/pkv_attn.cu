@@ -223,6 +223,31 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     const long long range_lo = min(total, static_cast<long long>(blockIdx.x) * chunk);
     const long long range_hi = min(total, range_lo + chunk);
 
+    // Warm L2 with the block-table entries and query rows of every piece of
+    // this CTA's range, so that the producer's reads of them later on are
+    // L2 hits rather than dependent DRAM round trips.
+    if (warp == kConsumerWarps && range_lo < range_hi) {
+        Cursor c = locate(scan, B, Hkv, range_lo);
+        for (long long xx = range_lo; xx < range_hi;) {
+            const int nb = run_blocks(scan, c.s);
+            const int len = static_cast<int>(min(static_cast<long long>(nb - c.blk), range_hi - xx));
+            const int32_t* t0 = p.block_tables + static_cast<size_t>(c.s) * p.max_blocks + c.blk;
+            const char* t1 = reinterpret_cast<const char*>(t0 + len);
+            const char* line = reinterpret_cast<const char*>(reinterpret_cast<uintptr_t>(t0) & ~uintptr_t(127));
+            for (const char* a = line + lane * 128; a < t1; a += 32 * 128) prefetch_l2(a);
+            const char* qrow = reinterpret_cast<const char*>(
+                p.q + (static_cast<size_t>(c.s) * p.num_q_heads + static_cast<size_t>(c.g) * G) * kDim);
+            if (lane < G * 2) prefetch_l2(qrow + lane * 128);
+            advance(c, scan, B, Hkv, len);
+            xx += len;
+        }
+    }
+
+    // Everything above reads only inputs that the kernels of a decode step
+    // (block copy, append) do not write; from here on the kernel may touch
+    // what they wrote (the KV cache), so wait for them when launched early.
+    griddep_wait();
+
     // Sequences with no context get a zero output row (CTA 0, consumer warps).
     if (blockIdx.x == 0 && warp < kConsumerWarps) {
         const int row_vec = p.num_q_heads * kDim / 8;
@@ -612,6 +637,90 @@ DeviceInfo device_info() {
     return d;
 }
 
+struct Launch {
+    CUtensorMap tm_k, tm_v;
+    Params prm;
+    int grid;
+    size_t smem;
+};
+
+// Validate pkv_attn_decode's arguments and build its launch.
+pkv_status prepare(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                   int max_blocks_per_seq, const int32_t* context_lens, int num_seqs, int num_q_heads,
+                   int num_kv_heads, int head_dim, int num_blocks, float scale, int num_ctas, void* workspace,
+                   size_t workspace_bytes, void* out, Launch* L) {
+    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !workspace || !out)
+        return PKV_EINVAL;
+    if (num_seqs < 1 || num_q_heads < 1 || num_kv_heads < 1 || num_blocks < 1 ||
+        max_blocks_per_seq < 1 || num_ctas < 0 || !std::isfinite(scale))
+        return PKV_EINVAL;
+    if (num_seqs > PKV_ATTN_MAX_SEQS || head_dim != PKV_ATTN_HEAD_DIM ||
+        num_q_heads % num_kv_heads != 0 || num_q_heads / num_kv_heads > PKV_ATTN_MAX_GROUP)
+        return PKV_EUNSUPPORTED;
+    if (static_cast<long long>(num_blocks) * num_kv_heads * PKV_BLOCK_TOKENS >= (1ll << 31) ||
+        static_cast<long long>(num_seqs) * max_blocks_per_seq >= (1ll << 31) ||
+        static_cast<long long>(max_blocks_per_seq) * PKV_BLOCK_TOKENS >= (1ll << 31) ||
+        static_cast<long long>(num_kv_heads) * num_seqs * max_blocks_per_seq >= (1ll << 31))
+        return PKV_ERANGE;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return PKV_EINVAL;
+    const DeviceInfo d = device_info();
+    if (!d.ok) return PKV_ECUDA;
+    int grid = num_ctas > 0 ? num_ctas : d.grid;
+    const size_t fixed = kWsHeader + align256(static_cast<size_t>(num_seqs) * num_kv_heads * 4);
+    if (workspace_bytes < fixed + 2 * kPartialFloats * 4) return PKV_EINVAL;
+    const long long fit = static_cast<long long>((workspace_bytes - fixed) / (2 * kPartialFloats * 4));
+    if (grid > fit) {
+        if (num_ctas > 0) return PKV_EINVAL;
+        grid = static_cast<int>(fit);
+    }
+    if (!make_cache_map(&L->tm_k, k_cache, num_blocks, num_kv_heads) ||
+        !make_cache_map(&L->tm_v, v_cache, num_blocks, num_kv_heads))
+        return PKV_ECUDA;
+    Params& prm = L->prm;
+    prm.q = static_cast<const __nv_bfloat16*>(q);
+    prm.out = static_cast<__nv_bfloat16*>(out);
+    prm.block_tables = block_tables;
+    prm.context_lens = context_lens;
+    prm.num_seqs = num_seqs;
+    prm.num_q_heads = num_q_heads;
+    prm.num_kv_heads = num_kv_heads;
+    prm.group = num_q_heads / num_kv_heads;
+    prm.max_blocks = max_blocks_per_seq;
+    prm.num_blocks = num_blocks;
+    prm.scale_log2 = scale * 1.4426950408889634f;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    prm.err = reinterpret_cast<uint32_t*>(ws);
+    prm.counters = reinterpret_cast<int*>(ws + kWsHeader);
+    prm.partials = reinterpret_cast<float*>(ws + fixed);
+    L->grid = grid;
+    L->smem = smem_bytes(num_seqs);
+    return PKV_OK;
+}
+
+// early: launch with programmatic stream serialization, so that the kernel's
+// prologue overlaps the previous kernel on the stream (see griddep_wait).
+pkv_status launch(const Launch& L, cudaStream_t stream, bool early) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(L.grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = L.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = early ? 1 : 0;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, decode_kernel, L.tm_k, L.tm_v, L.prm);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        record_cuda_error(e);
+        return PKV_ECUDA;
+    }
+    return PKV_OK;
+}
+
 }  // namespace attn
 }  // namespace pkv
 
@@ -647,62 +756,43 @@ pkv_status pkv_attn_decode(const void* q, const void* k_cache, const void* v_cac
                            int num_kv_heads, int head_dim, int num_blocks, float scale,
                            int num_ctas, void* workspace, size_t workspace_bytes, void* out,
                            void* stream) {
-    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !workspace || !out)
+    attn::Launch L;
+    const pkv_status st = attn::prepare(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                                        num_seqs, num_q_heads, num_kv_heads, head_dim, num_blocks, scale,
+                                        num_ctas, workspace, workspace_bytes, out, &L);
+    if (st != PKV_OK) return st;
+    return attn::launch(L, as_stream(stream), false);
+}
+
+pkv_status pkv_decode_step(const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                           int num_new_tokens, const int32_t* src_dst_pairs, int num_pairs,
+                           void* k_cache, void* v_cache, int num_blocks, const void* q,
+                           const int32_t* block_tables, int max_blocks_per_seq,
+                           const int32_t* context_lens, int num_seqs, int num_q_heads,
+                           int num_kv_heads, int head_dim, float scale, int num_ctas, void* workspace,
+                           size_t workspace_bytes, void* out, uint32_t* device_error, void* stream) {
+    if (num_new_tokens < 0 || num_pairs < 0) return PKV_EINVAL;
+    // Validate the whole step before launching any part of it.
+    attn::Launch L;
+    pkv_status st = attn::prepare(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                                  num_seqs, num_q_heads, num_kv_heads, head_dim, num_blocks, scale, num_ctas,
+                                  workspace, workspace_bytes, out, &L);
+    if (st != PKV_OK) return st;
+    if (num_pairs > 65535) return PKV_ERANGE;
+    if ((num_pairs > 0 && !src_dst_pairs) || (num_new_tokens > 0 && (!k_new || !v_new || !slot_mapping)))
         return PKV_EINVAL;
-    if (num_seqs < 1 || num_q_heads < 1 || num_kv_heads < 1 || num_blocks < 1 ||
-        max_blocks_per_seq < 1 || num_ctas < 0 || !std::isfinite(scale))
-        return PKV_EINVAL;
-    if (num_seqs > PKV_ATTN_MAX_SEQS || head_dim != PKV_ATTN_HEAD_DIM ||
-        num_q_heads % num_kv_heads != 0 || num_q_heads / num_kv_heads > PKV_ATTN_MAX_GROUP)
-        return PKV_EUNSUPPORTED;
-    if (static_cast<long long>(num_blocks) * num_kv_heads * PKV_BLOCK_TOKENS >= (1ll << 31) ||
-        static_cast<long long>(num_seqs) * max_blocks_per_seq >= (1ll << 31) ||
-        static_cast<long long>(max_blocks_per_seq) * PKV_BLOCK_TOKENS >= (1ll << 31) ||
-        static_cast<long long>(num_kv_heads) * num_seqs * max_blocks_per_seq >= (1ll << 31))
-        return PKV_ERANGE;
-    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
-        (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
-        return PKV_EINVAL;
-    const attn::DeviceInfo d = attn::device_info();
-    if (!d.ok) return PKV_ECUDA;
-    int grid = num_ctas > 0 ? num_ctas : d.grid;
-    const size_t fixed = attn::kWsHeader + attn::align256(static_cast<size_t>(num_seqs) * num_kv_heads * 4);
-    if (workspace_bytes < fixed + 2 * attn::kPartialFloats * 4) return PKV_EINVAL;
-    const long long fit = static_cast<long long>((workspace_bytes - fixed) / (2 * attn::kPartialFloats * 4));
-    if (grid > fit) {
-        if (num_ctas > 0) return PKV_EINVAL;
-        grid = static_cast<int>(fit);
+    if (num_new_tokens > 0 && (!aligned16(k_new) || !aligned16(v_new))) return PKV_EINVAL;
+    if (num_pairs > 0) {
+        st = pkv_block_copy(k_cache, v_cache, src_dst_pairs, num_pairs, num_blocks, num_kv_heads, head_dim,
+                            device_error, stream);
+        if (st != PKV_OK) return st;
     }
-
-    CUtensorMap tm_k, tm_v;
-    if (!attn::make_cache_map(&tm_k, k_cache, num_blocks, num_kv_heads) ||
-        !attn::make_cache_map(&tm_v, v_cache, num_blocks, num_kv_heads))
-        return PKV_ECUDA;
-
-    attn::Params prm;
-    prm.q = static_cast<const __nv_bfloat16*>(q);
-    prm.out = static_cast<__nv_bfloat16*>(out);
-    prm.block_tables = block_tables;
-    prm.context_lens = context_lens;
-    prm.num_seqs = num_seqs;
-    prm.num_q_heads = num_q_heads;
-    prm.num_kv_heads = num_kv_heads;
-    prm.group = num_q_heads / num_kv_heads;
-    prm.max_blocks = max_blocks_per_seq;
-    prm.num_blocks = num_blocks;
-    prm.scale_log2 = scale * 1.4426950408889634f;
-    uint8_t* ws = static_cast<uint8_t*>(workspace);
-    prm.err = reinterpret_cast<uint32_t*>(ws);
-    prm.counters = reinterpret_cast<int*>(ws + attn::kWsHeader);
-    prm.partials = reinterpret_cast<float*>(ws + fixed);
-
-    attn::decode_kernel<<<grid, attn::kThreads, attn::smem_bytes(num_seqs), as_stream(stream)>>>(tm_k, tm_v, prm);
-    const cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) {
-        record_cuda_error(e);
-        return PKV_ECUDA;
+    if (num_new_tokens > 0) {
+        st = pkv_append(k_new, v_new, slot_mapping, num_new_tokens, k_cache, v_cache, num_blocks, num_kv_heads,
+                        head_dim, device_error, stream);
+        if (st != PKV_OK) return st;
     }
-    return PKV_OK;
+    return attn::launch(L, as_stream(stream), num_pairs > 0 || num_new_tokens > 0);
 }
 
 }  // extern "C"

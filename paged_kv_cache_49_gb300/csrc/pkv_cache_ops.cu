@@ -14,6 +14,7 @@
 #include <cstring>
 
 #include "pkv_internal.h"
+#include "pkv_ptx.cuh"
 
 namespace pkv {
 
@@ -36,6 +37,7 @@ append_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
               const int64_t* __restrict__ slots, long long rows, int hkv, int vec_per_row,
               long long slot_limit, uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
               uint32_t* err) {
+    griddep_launch_dependents();  // the attention of a decode step may start its prologue
     const long long per_tensor = rows * vec_per_row;
     const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
     for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < 2 * per_tensor;
@@ -64,6 +66,7 @@ append_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
 __global__ void __launch_bounds__(kThreads)
 copy_kernel(uint4* __restrict__ k_cache, uint4* __restrict__ v_cache, const int32_t* __restrict__ pairs,
             int num_blocks, long long vec_per_block, uint32_t* err) {
+    griddep_launch_dependents();
     const int pr = blockIdx.y;
     const int src = __ldg(pairs + 2 * pr);
     const int dst = __ldg(pairs + 2 * pr + 1);

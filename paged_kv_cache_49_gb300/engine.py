@@ -127,8 +127,13 @@ class PagedKVEngine:
             workspace=nat.AttentionWorkspace(len(seq_ids), self.num_kv_heads, device=dev))
 
     def run_step(self, sb: StepBuffers, scale: float, num_ctas: int = 0, stream=None) -> torch.Tensor:
-        """The device part of a decode step: copy-on-write copies, append,
-        attention. Idempotent for fixed inputs."""
+        """The device part of a decode step -- copy-on-write copies, append,
+        attention -- as one library call. Idempotent for fixed inputs."""
+        return nat.decode_step(sb.q, sb.k, sb.v, sb.slots, sb.pairs, self.k_cache, self.v_cache, sb.tables,
+                               sb.ctx, scale, sb.out, sb.workspace, self.error, num_ctas, stream)
+
+    def run_step_separate(self, sb: StepBuffers, scale: float, num_ctas: int = 0, stream=None) -> torch.Tensor:
+        """The same step as three separate library calls."""
         if sb.num_pairs:
             nat.block_copy(self.k_cache, self.v_cache, sb.pairs, self.error, stream)
         nat.append(sb.k, sb.v, sb.slots, self.k_cache, self.v_cache, self.error, stream)

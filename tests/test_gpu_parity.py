@@ -62,6 +62,10 @@ def _run_workload(pkv, w, num_ctas_list=(0,)):
         torch.cuda.synchronize()
         assert eng.read_errors(sb) == 0
         results[n] = _close(out, ref["out"])
+        fused = out.clone()
+        sep = eng.run_step_separate(sb, w.scale, num_ctas=n)
+        torch.cuda.synchronize()
+        assert torch.equal(fused, sep)
     # the pools after the step (copies, appends, history) are bit-exact
     assert np.array_equal(pkv.bits_from_bf16(eng.k_cache), ref["k_pool"])
     assert np.array_equal(pkv.bits_from_bf16(eng.v_cache), ref["v_pool"])
