@@ -411,7 +411,7 @@ def run_ours(args):
         "config": {"workload": w.name, "batch": B, "q_heads": w.num_q_heads, "kv_heads": w.num_kv_heads,
                    "head_dim": w.head_dim, "block_tokens": 16, "context_tokens": int(ctx.sum()),
                    "pool_blocks": w.pool_blocks, "cow_pairs_per_step": sb.num_pairs,
-                   "num_ctas": args.num_ctas or pkv.default_ctas(), "l2": "flushed before each timed launch (256 MiB write, then 256 MiB read: cold and clean)",
+                   "num_ctas": args.num_ctas or pkv.default_ctas(B), "l2": "flushed before each timed launch (256 MiB write, then 256 MiB read: cold and clean)",
                    "parallelism": f"replicas x{world}"},
         "clocks": clk.summary(), "e2e": e2e, "gpu_launches": launches, "roofline": roofline,
         "cpu_baseline": cpu,

@@ -192,8 +192,10 @@ pkv_status pkv_decode_step(const void* k_new, const void* v_new, const int64_t* 
                            int num_kv_heads, int head_dim, float scale, int num_ctas, void* workspace,
                            size_t workspace_bytes, void* out, uint32_t* device_error, void* stream);
 
-/* Number of persistent CTAs pkv_attn_decode launches when num_ctas == 0. */
-int pkv_attn_default_ctas(void);
+/* Number of persistent CTAs pkv_attn_decode launches for num_seqs sequences
+ * when num_ctas == 0 (every CTA that fits on the current device at once);
+ * 0 on error. */
+int pkv_attn_default_ctas(int num_seqs);
 
 /*
  * pkv_attn_decode_static -- pkv_attn_decode without a workspace argument, for

@@ -86,7 +86,7 @@ def _load() -> ctypes.CDLL:
         "pkv_attn_workspace_size": (sz, [i32, i32]),
         "pkv_attn_workspace_init": (i32, [vp, sz, vp]),
         "pkv_attn_decode": (i32, [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, f32, i32, vp, sz, vp, vp]),
-        "pkv_attn_default_ctas": (i32, []),
+        "pkv_attn_default_ctas": (i32, [i32]),
         "pkv_attn_decode_static": (i32, [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, f32, vp, vp, vp]),
         "pkv_decode_step": (i32, [vp, vp, vp, i32, vp, i32, vp, vp, i32, vp, vp, i32, vp, i32, i32, i32, i32,
                                   f32, i32, vp, sz, vp, vp, vp]),
@@ -191,8 +191,8 @@ def block_copy(k_cache, v_cache, pairs, device_error=None, stream=None) -> None:
                                _ptr(device_error), _stream(stream)), "pkv_block_copy")
 
 
-def default_ctas() -> int:
-    return int(_lib.pkv_attn_default_ctas())
+def default_ctas(num_seqs: int) -> int:
+    return int(_lib.pkv_attn_default_ctas(num_seqs))
 
 
 class AttentionWorkspace:

@@ -17,21 +17,25 @@
 //    output) and the CTA that finishes a pair's last piece merges them with a
 //    log-sum-exp rescale ("last arrival merges": one atomic counter per pair,
 //    no waiting on other CTAs, reset by the merger).
-//  * Data movement. One producer warp walks the range, reads block ids from
-//    the table, and issues TMA tile loads (two 16 x 64 bf16 boxes per 4 KiB K
-//    or V block, 128-byte swizzle, L2 evict-first) into an 8-stage ring of
-//    shared memory, each stage one block of K and V. The query rows of a
-//    piece arrive by one bulk copy into a 4-slot ring.
-//  * Math. Four consumer warps take the ring's blocks round robin. Per block:
-//    S^T[16 tokens x 8 heads] = K Q^T on the tensor cores (mma.sync m16n8k16,
-//    bf16 in, fp32 out, K fragments by ldmatrix from the swizzled stage), an
-//    online softmax in fp32 (max over tokens by shuffles, exp2 in the log2
-//    domain), P cast to bf16 and transposed in registers (movmatrix), then
-//    O^T[128 dims x 8 heads] += V^T P^T (V fragments by ldmatrix.trans). The
-//    GQA group of up to 8 query heads is the mma's N dimension, so each K/V
-//    byte is read once for the whole group. The softmax denominator sums the
-//    bf16-rounded weights that multiply V, so the output is an exact convex
-//    combination of V rows up to fp32 rounding.
+//  * Roles. Warp 4 produces: it walks the range, reads block ids from the
+//    table, and issues TMA tile loads (two 16 x 64 bf16 boxes per 4 KiB K or V
+//    block, 128-byte swizzle, L2 evict-first) into an 8-stage ring of shared
+//    memory, one block of K and V per stage; the query rows of a piece arrive
+//    by one bulk copy into a 2-slot ring. Warps 0-3 consume the ring's blocks,
+//    block i of the CTA's stream going to warp i % 4. Warp 5 merges: at the end of a piece the consumers drop their
+//    softmax states into a double-buffered slot and move on at once; the merge
+//    warp combines them, writes the output row (or the partial, then the
+//    cross-CTA merge), so the ring keeps streaming across piece boundaries.
+//  * Math, per block and consumer warp: S^T[16 tokens x 8 heads] = K Q^T on
+//    the tensor cores (mma.sync m16n8k16, bf16 in, fp32 out, K fragments by
+//    ldmatrix from the swizzled stage), an online softmax in fp32 (max over
+//    tokens by shuffles, exp2 in the log2 domain), P cast to bf16 and
+//    transposed in registers (movmatrix), then O^T[128 dims x 8 heads] +=
+//    V^T P^T (V fragments by ldmatrix.trans). The GQA group of up to 8 query
+//    heads is the mma's N dimension, so each K/V byte is read once for the
+//    whole group. The softmax denominator sums the bf16-rounded weights that
+//    multiply V, so the output is an exact convex combination of V rows up to
+//    fp32 rounding.
 //  * Tokens past the context in the last block are masked: their scores are
 //    set to -inf and their V values to zero before the mma, so unwritten
 //    (even non-finite) slots never reach the output.
@@ -55,23 +59,30 @@ constexpr int kDim = PKV_ATTN_HEAD_DIM;  // head dim
 constexpr int kMaxG = PKV_ATTN_MAX_GROUP;
 constexpr int kConsumerWarps = 4;
 constexpr int kConsumers = kConsumerWarps * 32;
-constexpr int kThreads = kConsumers + 32;
+constexpr int kProducerWarp = kConsumerWarps;
+constexpr int kMergeWarp = kConsumerWarps + 1;
+constexpr int kThreads = kConsumers + 64;
 constexpr int kStages = 8;
-constexpr int kQSlots = 4;
+static_assert(kStages % kConsumerWarps == 0, "each stage must map to one consumer warp");
+static_assert((kConsumerWarps & (kConsumerWarps - 1)) == 0, "consumer warp count is a power of two");
+constexpr int kQSlots = 2;
+constexpr int kMergeSlots = 2;
 constexpr int kHalfBytes = kTok * 64 * 2;  // one 16 x 64 bf16 box
 constexpr int kBlockBytes = 2 * kHalfBytes;  // one K (or V) block of one KV head
 constexpr int kStageBytes = 2 * kBlockBytes;
 constexpr int kQBytes = kMaxG * kDim * 2;
 constexpr int kORow = 132;  // floats per head row of merge buffers and partials
 constexpr int kPartialFloats = kMaxG * kORow;
+constexpr int kMergeOFloats = kConsumerWarps * kMaxG * kORow;  // one merge slot
+constexpr int kMergeMLFloats = kConsumerWarps * kMaxG;
 
 constexpr int kOffStages = 0;
 constexpr int kOffQ = kOffStages + kStages * kStageBytes;
 constexpr int kOffO = kOffQ + kQSlots * kQBytes;
-constexpr int kOffM = kOffO + kConsumerWarps * kMaxG * kORow * 4;
-constexpr int kOffL = kOffM + kConsumerWarps * kMaxG * 4;
-constexpr int kOffBar = kOffL + kConsumerWarps * kMaxG * 4;
-constexpr int kNumBars = 2 * kStages + 2 * kQSlots;
+constexpr int kOffM = kOffO + kMergeSlots * kMergeOFloats * 4;
+constexpr int kOffL = kOffM + kMergeSlots * kMergeMLFloats * 4;
+constexpr int kOffBar = kOffL + kMergeSlots * kMergeMLFloats * 4;
+constexpr int kNumBars = 2 * kStages + 2 * kQSlots + 2 * kMergeSlots;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kOffScan = kOffMisc + 64;
 
@@ -164,14 +175,18 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
 
     int* scan = reinterpret_cast<int*>(smem + kOffScan);
     int* misc = reinterpret_cast<int*>(smem + kOffMisc);
-    volatile int* abort_flag = misc;      // misc[0]
-    volatile int* merge_flag = misc + 1;  // misc[1]
-    int* warp_tot = misc + 8;             // misc[8 .. 8 + 5)
+    volatile int* abort_flag = misc;  // misc[0]
+    int* warp_tot = misc + 8;         // misc[8 .. 8 + kThreads / 32)
+    float* sm_o = reinterpret_cast<float*>(smem + kOffO);
+    float* sm_m = reinterpret_cast<float*>(smem + kOffM);
+    float* sm_l = reinterpret_cast<float*>(smem + kOffL);
     const uint32_t bar0 = smem_u32(smem + kOffBar);
     auto full_bar = [&](int i) { return bar0 + 8u * i; };
     auto empty_bar = [&](int i) { return bar0 + 8u * (kStages + i); };
     auto qfull_bar = [&](int i) { return bar0 + 8u * (2 * kStages + i); };
     auto qempty_bar = [&](int i) { return bar0 + 8u * (2 * kStages + kQSlots + i); };
+    auto mfull_bar = [&](int i) { return bar0 + 8u * (2 * kStages + 2 * kQSlots + i); };
+    auto mempty_bar = [&](int i) { return bar0 + 8u * (2 * kStages + 2 * kQSlots + kMergeSlots + i); };
 
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) {
@@ -182,8 +197,11 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             mbar_init(qfull_bar(i), 1);
             mbar_init(qempty_bar(i), kConsumerWarps);
         }
+        for (int i = 0; i < kMergeSlots; ++i) {
+            mbar_init(mfull_bar(i), kConsumers);
+            mbar_init(mempty_bar(i), 32);
+        }
         misc[0] = 0;
-        misc[1] = 0;
         fence_barrier_init();
     }
 
@@ -226,7 +244,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     // Warm L2 with the block-table entries and query rows of every piece of
     // this CTA's range, so that the producer's reads of them later on are
     // L2 hits rather than dependent DRAM round trips.
-    if (warp == kConsumerWarps && range_lo < range_hi) {
+    if (warp == kProducerWarp && range_lo < range_hi) {
         Cursor c = locate(scan, B, Hkv, range_lo);
         for (long long xx = range_lo; xx < range_hi;) {
             const int nb = run_blocks(scan, c.s);
@@ -248,10 +266,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     // what they wrote (the KV cache), so wait for them when launched early.
     griddep_wait();
 
-    // Sequences with no context get a zero output row (CTA 0, consumer warps).
-    if (blockIdx.x == 0 && warp < kConsumerWarps) {
+    // Sequences with no context get a zero output row (CTA 0, merge warp).
+    if (blockIdx.x == 0 && warp == kMergeWarp) {
         const int row_vec = p.num_q_heads * kDim / 8;
-        for (int s = warp; s < B; s += kConsumerWarps) {
+        for (int s = 0; s < B; ++s) {
             if (run_blocks(scan, s) != 0) continue;
             uint4* dst = reinterpret_cast<uint4*>(p.out + static_cast<size_t>(s) * p.num_q_heads * kDim);
             for (int i = lane; i < row_vec; i += 32) dst[i] = make_uint4(0, 0, 0, 0);
@@ -259,7 +277,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     }
     if (range_lo >= range_hi) return;
 
-    if (warp == kConsumerWarps) {
+    if (warp == kProducerWarp) {
         // ======================= producer warp =======================
         const uint64_t policy = policy_evict_first();
         if (lane == 0) {
@@ -317,12 +335,11 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             advance(cur, scan, B, Hkv, len);
             x += len;
         }
-        // If the pipeline was abandoned, wait (bounded) for the copies still in
-        // flight so that no TMA lands in shared memory after the CTA exits.
-        // Copies were issued in order up to the first failed wait, so the ones
-        // that can still be in flight are the last kStages blocks and the last
-        // kQSlots query loads issued.
-        if (lane == 0 && *abort_flag) {
+        // Before this warp exits, wait (bounded, even after an abort) for the
+        // copies it issued that may still be in flight, so that no TMA lands in
+        // shared memory after the CTA has exited. Copies were issued in order,
+        // so those are at most the last kStages blocks and kQSlots query loads.
+        if (lane == 0) {
             volatile int never = 0;
             for (long long i = max(0ll, issued - kStages); i < issued; ++i)
                 mbar_wait(full_bar(static_cast<int>(i % kStages)),
@@ -333,12 +350,105 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         return;
     }
 
+    if (warp == kMergeWarp) {
+        // ========================= merge warp =========================
+        // Lane l owns dims [4l, 4l + 4) of every head of the piece.
+        const float NEG_INF = -INFINITY;
+        const int d0 = lane * 4;
+        Cursor cur = locate(scan, B, Hkv, range_lo);
+        long long x = range_lo;
+        int piece = 0;
+        while (x < range_hi) {
+            const int s = cur.s, g = cur.g;
+            const int nb = run_blocks(scan, s);
+            const int len = static_cast<int>(min(static_cast<long long>(nb - cur.blk), range_hi - x));
+            const long long seg_start = static_cast<long long>(Hkv) * (scan[s] - nb) + static_cast<long long>(g) * nb;
+            const int i0 = static_cast<int>(seg_start / chunk);
+            const int i1 = static_cast<int>((seg_start + nb - 1) / chunk);
+            const int pieces = i1 - i0 + 1;
+            const int ms = piece & 1;
+            mbar_wait(mfull_bar(ms), static_cast<uint32_t>((piece >> 1) & 1), abort_flag, p.err);
+            const float* mo = sm_o + ms * kMergeOFloats;
+            const float* mm = sm_m + ms * kMergeMLFloats;
+            const float* ml = sm_l + ms * kMergeMLFloats;
+            __nv_bfloat16* out_base =
+                p.out + (static_cast<size_t>(s) * p.num_q_heads + static_cast<size_t>(g) * G) * kDim + d0;
+            float* part = p.partials + (static_cast<size_t>(blockIdx.x) * 2 + (x == range_lo ? 0 : 1)) * kPartialFloats;
+            for (int h = 0; h < G; ++h) {
+                float M = NEG_INF;
+#pragma unroll
+                for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mm[w * kMaxG + h]);
+                float L = 0.f;
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int w = 0; w < kConsumerWarps; ++w) {
+                    const float mw = mm[w * kMaxG + h];
+                    if (mw == NEG_INF) continue;  // this warp got no block of the piece
+                    const float f = ex2(mw - M);
+                    L += f * ml[w * kMaxG + h];
+                    const float4 u = *reinterpret_cast<const float4*>(mo + (w * kMaxG + h) * kORow + d0);
+                    acc.x += f * u.x; acc.y += f * u.y; acc.z += f * u.z; acc.w += f * u.w;
+                }
+                if (pieces == 1) {
+                    const float inv = 1.f / L;
+                    uint2 w2;
+                    w2.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+                    w2.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+                    *reinterpret_cast<uint2*>(out_base + static_cast<size_t>(h) * kDim) = w2;
+                } else {
+                    *reinterpret_cast<float4*>(part + h * kORow + d0) = acc;
+                    if (lane == 0) {
+                        part[h * kORow + kDim] = M;
+                        part[h * kORow + kDim + 1] = L;
+                    }
+                }
+            }
+            mbar_arrive(mempty_bar(ms));  // the consumers may reuse this slot
+            if (pieces > 1) {
+                __threadfence();
+                __syncwarp();
+                int old = 0;
+                if (lane == 0) old = atomicAdd(p.counters + s * Hkv + g, 1);
+                old = __shfl_sync(0xffffffffu, old, 0);
+                if (old == pieces - 1) {  // last piece of the pair to finish: merge them all
+                    __threadfence();
+                    const int slot0 = (seg_start == static_cast<long long>(i0) * chunk) ? 0 : 1;
+                    for (int h = 0; h < G; ++h) {
+                        float Mx = NEG_INF;
+                        for (int i = i0; i <= i1; ++i) {
+                            const float* pi = p.partials +
+                                (static_cast<size_t>(i) * 2 + (i == i0 ? slot0 : 0)) * kPartialFloats + h * kORow;
+                            Mx = fmaxf(Mx, __ldcg(pi + kDim));
+                        }
+                        float L = 0.f;
+                        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                        for (int i = i0; i <= i1; ++i) {
+                            const float* pi = p.partials +
+                                (static_cast<size_t>(i) * 2 + (i == i0 ? slot0 : 0)) * kPartialFloats + h * kORow;
+                            const float f = ex2(__ldcg(pi + kDim) - Mx);
+                            L += f * __ldcg(pi + kDim + 1);
+                            const float4 u = __ldcg(reinterpret_cast<const float4*>(pi + d0));
+                            acc.x += f * u.x; acc.y += f * u.y; acc.z += f * u.z; acc.w += f * u.w;
+                        }
+                        const float inv = 1.f / L;
+                        uint2 w2;
+                        w2.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+                        w2.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+                        *reinterpret_cast<uint2*>(out_base + static_cast<size_t>(h) * kDim) = w2;
+                    }
+                    if (lane == 0) p.counters[s * Hkv + g] = 0;  // ready for the next launch
+                }
+            }
+            ++piece;
+            advance(cur, scan, B, Hkv, len);
+            x += len;
+        }
+        return;
+    }
+
     // ========================= consumer warps =========================
     const int r = lane >> 2;  // mma group id: token row / head column owner
     const int c = lane & 3;   // thread in group
-    float* sm_o = reinterpret_cast<float*>(smem + kOffO);
-    float* sm_m = reinterpret_cast<float*>(smem + kOffM);
-    float* sm_l = reinterpret_cast<float*>(smem + kOffL);
     const uint32_t stage_base = smem_u32(smem + kOffStages);
     // ldmatrix address pieces (row of the 16 x 16 tile each lane points at)
     const uint32_t k_row_off = static_cast<uint32_t>(lane & 15) * 128u;
@@ -352,10 +462,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     Cursor cur = locate(scan, B, Hkv, range_lo);
     long long x = range_lo;
     long long gidx0 = 0;
-    int qslot = 0;
+    int qslot = 0, piece = 0;
     uint32_t qphase = 0;
     while (x < range_hi) {
-        const int s = cur.s, g = cur.g, blk0 = cur.blk;
+        const int s = cur.s, blk0 = cur.blk;
         const int nb = run_blocks(scan, s);
         const int len = static_cast<int>(min(static_cast<long long>(nb - blk0), range_hi - x));
         const int ctx = clamped_ctx(p, s);
@@ -380,7 +490,14 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
 #pragma unroll
         for (int j = 0; j < 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
 
-        for (int jb = warp; jb < len; jb += kConsumerWarps) {
+        // Block gi of this CTA's stream goes to warp gi % 4, so every stage
+        // (gi % 8) is always consumed by the same warp, which waits on each of
+        // its phases in turn. Handing blocks out per piece instead would let a
+        // warp wait on a stage whose previous fill, owned by another warp, is
+        // still in flight (TMA fills complete out of order); a parity wait
+        // would then see the previous phase's parity and pass too early.
+        for (int jb = (warp - static_cast<int>(gidx0 % kConsumerWarps)) & (kConsumerWarps - 1); jb < len;
+             jb += kConsumerWarps) {
             const long long gi = gidx0 + jb;
             const int st = static_cast<int>(gi % kStages);
             mbar_wait(full_bar(st), static_cast<uint32_t>((gi / kStages) & 1), abort_flag, p.err);
@@ -451,123 +568,31 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         }
         gidx0 += len;
 
-        // ---- merge the consumer warps' states for this piece ----
+        // ---- hand this warp's state for the piece to the merge warp ----
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
             l0 += __shfl_xor_sync(0xffffffffu, l0, off);
             l1 += __shfl_xor_sync(0xffffffffu, l1, off);
         }
+        const int ms = piece & 1;
+        mbar_wait(mempty_bar(ms), static_cast<uint32_t>(((piece >> 1) & 1) ^ 1), abort_flag, p.err);
+        float* o0 = sm_o + ms * kMergeOFloats + (warp * kMaxG + 2 * c) * kORow + r;
+        float* o1 = o0 + kORow;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            o0[16 * j] = o[j][0];
+            o1[16 * j] = o[j][1];
+            o0[16 * j + 8] = o[j][2];
+            o1[16 * j + 8] = o[j][3];
+        }
         if (r == 0) {
-            sm_m[warp * kMaxG + 2 * c] = m0;
-            sm_m[warp * kMaxG + 2 * c + 1] = m1;
-            sm_l[warp * kMaxG + 2 * c] = l0;
-            sm_l[warp * kMaxG + 2 * c + 1] = l1;
+            sm_m[ms * kMergeMLFloats + warp * kMaxG + 2 * c] = m0;
+            sm_m[ms * kMergeMLFloats + warp * kMaxG + 2 * c + 1] = m1;
+            sm_l[ms * kMergeMLFloats + warp * kMaxG + 2 * c] = l0;
+            sm_l[ms * kMergeMLFloats + warp * kMaxG + 2 * c + 1] = l1;
         }
-        named_barrier_sync(1, kConsumers);
-        {
-            float M0 = NEG_INF, M1 = NEG_INF;
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) {
-                M0 = fmaxf(M0, sm_m[w * kMaxG + 2 * c]);
-                M1 = fmaxf(M1, sm_m[w * kMaxG + 2 * c + 1]);
-            }
-            const float f0 = m0 == NEG_INF ? 0.f : ex2(m0 - M0);
-            const float f1 = m1 == NEG_INF ? 0.f : ex2(m1 - M1);
-            float* o0 = sm_o + (warp * kMaxG + 2 * c) * kORow + r;
-            float* o1 = o0 + kORow;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                o0[16 * j] = o[j][0] * f0;
-                o1[16 * j] = o[j][1] * f1;
-                o0[16 * j + 8] = o[j][2] * f0;
-                o1[16 * j + 8] = o[j][3] * f1;
-            }
-        }
-        named_barrier_sync(1, kConsumers);
-
-        const long long seg_start = static_cast<long long>(Hkv) * (scan[s] - nb) + static_cast<long long>(g) * nb;
-        const long long seg_end = seg_start + nb;
-        const int i0 = static_cast<int>(seg_start / chunk);
-        const int i1 = static_cast<int>((seg_end - 1) / chunk);
-        const int pieces = i1 - i0 + 1;
-        const int h = tid >> 4;
-        const int d0 = (tid & 15) * 8;
-        __nv_bfloat16* out_row = p.out + (static_cast<size_t>(s) * p.num_q_heads + static_cast<size_t>(g) * G + h) * kDim + d0;
-        if (h < G) {
-            float Mh = NEG_INF;
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) Mh = fmaxf(Mh, sm_m[w * kMaxG + h]);
-            float Lh = 0.f;
-            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) {
-                const float mw = sm_m[w * kMaxG + h];
-                if (mw != NEG_INF) Lh += sm_l[w * kMaxG + h] * ex2(mw - Mh);
-                const float4* src = reinterpret_cast<const float4*>(sm_o + (w * kMaxG + h) * kORow + d0);
-                const float4 u = src[0], v = src[1];
-                acc[0] += u.x; acc[1] += u.y; acc[2] += u.z; acc[3] += u.w;
-                acc[4] += v.x; acc[5] += v.y; acc[6] += v.z; acc[7] += v.w;
-            }
-            if (pieces == 1) {
-                const float inv = 1.f / Lh;
-                uint4 w4;
-                w4.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-                w4.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-                w4.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
-                w4.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
-                *reinterpret_cast<uint4*>(out_row) = w4;
-            } else {
-                const int slot = (x == range_lo) ? 0 : 1;
-                float* part = p.partials + (static_cast<size_t>(blockIdx.x) * 2 + slot) * kPartialFloats + h * kORow;
-                reinterpret_cast<float4*>(part + d0)[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-                reinterpret_cast<float4*>(part + d0)[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
-                if ((tid & 15) == 0) {
-                    part[kDim] = Mh;
-                    part[kDim + 1] = Lh;
-                }
-            }
-        }
-        if (pieces > 1) {
-            __threadfence();
-            named_barrier_sync(1, kConsumers);
-            if (tid == 0) {
-                const int old = atomicAdd(p.counters + s * Hkv + g, 1);
-                *merge_flag = (old == pieces - 1);
-            }
-            named_barrier_sync(1, kConsumers);
-            if (*merge_flag) {
-                __threadfence();
-                if (h < G) {
-                    const int slot0 = (seg_start == static_cast<long long>(i0) * chunk) ? 0 : 1;
-                    float Mx = NEG_INF;
-                    for (int i = i0; i <= i1; ++i) {
-                        const float* part = p.partials + (static_cast<size_t>(i) * 2 + (i == i0 ? slot0 : 0)) * kPartialFloats + h * kORow;
-                        Mx = fmaxf(Mx, __ldcg(part + kDim));
-                    }
-                    float L = 0.f;
-                    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                    for (int i = i0; i <= i1; ++i) {
-                        const float* part = p.partials + (static_cast<size_t>(i) * 2 + (i == i0 ? slot0 : 0)) * kPartialFloats + h * kORow;
-                        const float f = ex2(__ldcg(part + kDim) - Mx);
-                        L += f * __ldcg(part + kDim + 1);
-                        const float4 u = __ldcg(reinterpret_cast<const float4*>(part + d0));
-                        const float4 v = __ldcg(reinterpret_cast<const float4*>(part + d0) + 1);
-                        acc[0] += f * u.x; acc[1] += f * u.y; acc[2] += f * u.z; acc[3] += f * u.w;
-                        acc[4] += f * v.x; acc[5] += f * v.y; acc[6] += f * v.z; acc[7] += f * v.w;
-                    }
-                    const float inv = 1.f / L;
-                    uint4 w4;
-                    w4.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-                    w4.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-                    w4.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
-                    w4.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
-                    *reinterpret_cast<uint4*>(out_row) = w4;
-                }
-                if (tid == 0) p.counters[s * Hkv + g] = 0;  // ready for the next launch
-            }
-        }
-        named_barrier_sync(1, kConsumers);  // merge buffers are free again
-
+        mbar_arrive(mfull_bar(ms));
+        ++piece;
         advance(cur, scan, B, Hkv, len);
         x += len;
     }
@@ -609,10 +634,9 @@ bool make_cache_map(CUtensorMap* map, const void* base, int num_blocks, int hkv)
 struct DeviceInfo {
     bool ok = false;
     int sm_count = 0;
-    int ctas_per_sm = 0;
-    int grid = 0;
 };
 
+// Per device, once: allow the kernel its largest dynamic shared memory.
 DeviceInfo device_info() {
     static std::mutex mu;
     static std::vector<DeviceInfo> cache;
@@ -622,19 +646,31 @@ DeviceInfo device_info() {
     if (static_cast<int>(cache.size()) <= dev) cache.resize(dev + 1);
     DeviceInfo& d = cache[dev];
     if (d.ok) return d;
-    const size_t smem_max = smem_bytes(PKV_ATTN_MAX_SEQS);
     cudaError_t e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem_max));
+                                         static_cast<int>(smem_bytes(PKV_ATTN_MAX_SEQS)));
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.ctas_per_sm, decode_kernel, kThreads, smem_max);
-    if (e != cudaSuccess || d.ctas_per_sm < 1) {
+    if (e != cudaSuccess) {
         record_cuda_error(e);
         return {};
     }
-    d.grid = d.sm_count * d.ctas_per_sm;
     d.ok = true;
     return d;
+}
+
+// Persistent CTAs for a batch of num_seqs: every CTA that fits at once (the
+// shared-memory prefix sum grows with num_seqs, so large batches may fit one
+// CTA per SM instead of two). 0 on error.
+int grid_for(int num_seqs) {
+    const DeviceInfo d = device_info();
+    if (!d.ok) return 0;
+    int per_sm = 0;
+    const cudaError_t e =
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel, kThreads, smem_bytes(num_seqs));
+    if (e != cudaSuccess || per_sm < 1) {
+        record_cuda_error(e);
+        return 0;
+    }
+    return d.sm_count * per_sm;
 }
 
 struct Launch {
@@ -665,9 +701,9 @@ pkv_status prepare(const void* q, const void* k_cache, const void* v_cache, cons
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
         (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
         return PKV_EINVAL;
-    const DeviceInfo d = device_info();
-    if (!d.ok) return PKV_ECUDA;
-    int grid = num_ctas > 0 ? num_ctas : d.grid;
+    const int auto_grid = grid_for(num_seqs);
+    if (auto_grid < 1) return PKV_ECUDA;
+    int grid = num_ctas > 0 ? num_ctas : auto_grid;
     const size_t fixed = kWsHeader + align256(static_cast<size_t>(num_seqs) * num_kv_heads * 4);
     if (workspace_bytes < fixed + 2 * kPartialFloats * 4) return PKV_EINVAL;
     const long long fit = static_cast<long long>((workspace_bytes - fixed) / (2 * kPartialFloats * 4));
@@ -728,16 +764,16 @@ using namespace pkv;
 
 extern "C" {
 
-int pkv_attn_default_ctas(void) {
-    const attn::DeviceInfo d = attn::device_info();
-    return d.ok ? d.grid : 0;
+int pkv_attn_default_ctas(int num_seqs) {
+    if (num_seqs < 1 || num_seqs > PKV_ATTN_MAX_SEQS) return 0;
+    return attn::grid_for(num_seqs);
 }
 
 size_t pkv_attn_workspace_size(int num_seqs, int num_kv_heads) {
-    if (num_seqs <= 0 || num_kv_heads <= 0) return 0;
-    const attn::DeviceInfo d = attn::device_info();
-    if (!d.ok) return 0;
-    return attn::workspace_bytes(num_seqs, num_kv_heads, d.grid);
+    if (num_seqs <= 0 || num_kv_heads <= 0 || num_seqs > PKV_ATTN_MAX_SEQS) return 0;
+    const int grid = attn::grid_for(num_seqs);
+    if (grid < 1) return 0;
+    return attn::workspace_bytes(num_seqs, num_kv_heads, grid);
 }
 
 pkv_status pkv_attn_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
@@ -866,11 +902,11 @@ extern "C" pkv_status pkv_attn_decode_static(const void* q, const void* k_cache,
         static_cast<long long>(num_kv_heads) * num_seqs * max_blocks_per_seq >= (1ll << 31))
         return PKV_ERANGE;
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return PKV_EINVAL;
-    const attn::DeviceInfo d = attn::device_info();
-    if (!d.ok) return PKV_ECUDA;
+    const int auto_grid = attn::grid_for(num_seqs);
+    if (auto_grid < 1) return PKV_ECUDA;
     uint8_t* scratch = attn::static_scratch_address();
     if (!scratch) return PKV_ECUDA;
-    const int grid = d.grid < attn::kStaticMaxCtas ? d.grid : attn::kStaticMaxCtas;
+    const int grid = auto_grid < attn::kStaticMaxCtas ? auto_grid : attn::kStaticMaxCtas;
 
     CUtensorMap tm_k, tm_v;
     if (!attn::make_cache_map(&tm_k, k_cache, num_blocks, num_kv_heads) ||
