@@ -354,6 +354,8 @@ def run_ours(args):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
     value = B * world / (ms * 1e-3)
+    step_stats = {"min": min(step_ms), "median": statistics.median(step_ms), "max": max(step_ms)}
+    attn_stats = {"min": min(attn_ms), "median": statistics.median(attn_ms), "max": max(attn_ms)}
     launches = args.steps * (2 + (1 if sb.num_pairs else 0)) + args.steps
     if eng.read_errors(sb):
         raise RuntimeError("device error word set during the timed steps")
@@ -414,6 +416,7 @@ def run_ours(args):
                    "num_ctas": args.num_ctas or pkv.default_ctas(B), "l2": "flushed before each timed launch (256 MiB write, then 256 MiB read: cold and clean)",
                    "parallelism": f"replicas x{world}"},
         "clocks": clk.summary(), "e2e": e2e, "gpu_launches": launches, "roofline": roofline,
+        "timing_ms": {"step": step_stats, "attention_alone": attn_stats},
         "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)

@@ -161,6 +161,57 @@ __device__ __forceinline__ int clamped_ctx(const Params& p, int s) {
     return c;
 }
 
+// One piece: blocks [blk, blk + len) of the run of (sequence s, KV head g),
+// whose run has nb blocks; start = its position on the line.
+struct Piece {
+    int s, g, blk, nb, len;
+    long long start;
+};
+
+// The pieces of one CTA's range in processing order: the range's last piece
+// first, then the others from the start of the range. A pair split between
+// neighbouring CTAs is the last piece of one and the first piece of the
+// next, so both halves are processed early and their merge overlaps the
+// streaming instead of landing on the kernel's tail.
+struct PieceWalk {
+    const int* scan;
+    int n, hkv;
+    long long range_lo, split, x, end;
+    int part;
+    Cursor c;
+
+    __device__ PieceWalk(const int* scan_, int n_, int hkv_, long long lo, long long hi)
+        : scan(scan_), n(n_), hkv(hkv_), range_lo(lo), part(0) {
+        const Cursor last = locate(scan, n, hkv, hi - 1);
+        const int nb = run_blocks(scan, last.s);
+        const long long seg = static_cast<long long>(hkv) * (scan[last.s] - nb) + static_cast<long long>(last.g) * nb;
+        split = seg > lo ? seg : lo;
+        x = split;
+        end = hi;
+        c = locate(scan, n, hkv, x);
+    }
+
+    __device__ bool next(Piece& pc) {
+        if (x >= end) {
+            if (part == 1 || split <= range_lo) return false;
+            part = 1;
+            x = range_lo;
+            end = split;
+            c = locate(scan, n, hkv, x);
+        }
+        const int nb = run_blocks(scan, c.s);
+        pc.s = c.s;
+        pc.g = c.g;
+        pc.blk = c.blk;
+        pc.nb = nb;
+        pc.len = static_cast<int>(min(static_cast<long long>(nb - c.blk), end - x));
+        pc.start = x;
+        advance(c, scan, n, hkv, pc.len);
+        x += pc.len;
+        return true;
+    }
+};
+
 __global__ void __launch_bounds__(kThreads, 2)
 decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
               const Params p) {
@@ -188,6 +239,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     auto mfull_bar = [&](int i) { return bar0 + 8u * (2 * kStages + 2 * kQSlots + i); };
     auto mempty_bar = [&](int i) { return bar0 + 8u * (2 * kStages + 2 * kQSlots + kMergeSlots + i); };
 
+    if (warp == kProducerWarp && lane == 0) {  // fetch the TMA descriptors while the plan runs
+        prefetch_tensormap(&tm_k);
+        prefetch_tensormap(&tm_v);
+    }
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) {
             mbar_init(full_bar(i), 1);
@@ -280,30 +335,25 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     if (warp == kProducerWarp) {
         // ======================= producer warp =======================
         const uint64_t policy = policy_evict_first();
-        if (lane == 0) {
-            prefetch_tensormap(&tm_k);
-            prefetch_tensormap(&tm_v);
-        }
-        Cursor cur = locate(scan, B, Hkv, range_lo);
-        long long x = range_lo;
+        PieceWalk walk(scan, B, Hkv, range_lo, range_hi);
+        Piece pc;
         int stage = 0, qslot = 0;
         uint32_t sphase = 0, qphase = 0;
         long long issued = 0;
         int q_issued = 0;
-        while (x < range_hi) {
-            const int nb = run_blocks(scan, cur.s);
-            const int len = static_cast<int>(min(static_cast<long long>(nb - cur.blk), range_hi - x));
+        while (walk.next(pc)) {
+            const int len = pc.len;
             if (lane == 0) {
                 if (mbar_wait(qempty_bar(qslot), qphase ^ 1u, abort_flag, p.err)) {
                     mbar_arrive_expect_tx(qfull_bar(qslot), G * kDim * 2);
                     const __nv_bfloat16* src =
-                        p.q + (static_cast<size_t>(cur.s) * p.num_q_heads + static_cast<size_t>(cur.g) * G) * kDim;
+                        p.q + (static_cast<size_t>(pc.s) * p.num_q_heads + static_cast<size_t>(pc.g) * G) * kDim;
                     bulk_load(smem_u32(smem + kOffQ + qslot * kQBytes), src, G * kDim * 2, qfull_bar(qslot));
                     ++q_issued;
                 }
             }
             if (++qslot == kQSlots) { qslot = 0; qphase ^= 1u; }
-            const int32_t* row = p.block_tables + static_cast<size_t>(cur.s) * p.max_blocks + cur.blk;
+            const int32_t* row = p.block_tables + static_cast<size_t>(pc.s) * p.max_blocks + pc.blk;
             for (int j0 = 0; j0 < len; j0 += 32) {
                 int bid = 0;
                 if (j0 + lane < len) {
@@ -320,7 +370,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                         if (mbar_wait(empty_bar(stage), sphase ^ 1u, abort_flag, p.err)) {
                             const uint32_t fb = full_bar(stage);
                             mbar_arrive_expect_tx(fb, kStageBytes);
-                            const int y = (b * Hkv + cur.g) * kTok;
+                            const int y = (b * Hkv + pc.g) * kTok;
                             const uint32_t dst = smem_u32(smem + kOffStages + stage * kStageBytes);
                             tma_load_2d(dst, &tm_k, 0, y, fb, policy);
                             tma_load_2d(dst + kHalfBytes, &tm_k, 64, y, fb, policy);
@@ -332,8 +382,6 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                     if (++stage == kStages) { stage = 0; sphase ^= 1u; }
                 }
             }
-            advance(cur, scan, B, Hkv, len);
-            x += len;
         }
         // Before this warp exits, wait (bounded, even after an abort) for the
         // copies it issued that may still be in flight, so that no TMA lands in
@@ -355,13 +403,11 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         // Lane l owns dims [4l, 4l + 4) of every head of the piece.
         const float NEG_INF = -INFINITY;
         const int d0 = lane * 4;
-        Cursor cur = locate(scan, B, Hkv, range_lo);
-        long long x = range_lo;
+        PieceWalk walk(scan, B, Hkv, range_lo, range_hi);
+        Piece pc;
         int piece = 0;
-        while (x < range_hi) {
-            const int s = cur.s, g = cur.g;
-            const int nb = run_blocks(scan, s);
-            const int len = static_cast<int>(min(static_cast<long long>(nb - cur.blk), range_hi - x));
+        while (walk.next(pc)) {
+            const int s = pc.s, g = pc.g, nb = pc.nb;
             const long long seg_start = static_cast<long long>(Hkv) * (scan[s] - nb) + static_cast<long long>(g) * nb;
             const int i0 = static_cast<int>(seg_start / chunk);
             const int i1 = static_cast<int>((seg_start + nb - 1) / chunk);
@@ -373,7 +419,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             const float* ml = sm_l + ms * kMergeMLFloats;
             __nv_bfloat16* out_base =
                 p.out + (static_cast<size_t>(s) * p.num_q_heads + static_cast<size_t>(g) * G) * kDim + d0;
-            float* part = p.partials + (static_cast<size_t>(blockIdx.x) * 2 + (x == range_lo ? 0 : 1)) * kPartialFloats;
+            float* part = p.partials + (static_cast<size_t>(blockIdx.x) * 2 + (pc.start == range_lo ? 0 : 1)) * kPartialFloats;
             for (int h = 0; h < G; ++h) {
                 float M = NEG_INF;
 #pragma unroll
@@ -413,35 +459,56 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 if (old == pieces - 1) {  // last piece of the pair to finish: merge them all
                     __threadfence();
                     const int slot0 = (seg_start == static_cast<long long>(i0) * chunk) ? 0 : 1;
-                    for (int h = 0; h < G; ++h) {
-                        float Mx = NEG_INF;
-                        for (int i = i0; i <= i1; ++i) {
-                            const float* pi = p.partials +
-                                (static_cast<size_t>(i) * 2 + (i == i0 ? slot0 : 0)) * kPartialFloats + h * kORow;
-                            Mx = fmaxf(Mx, __ldcg(pi + kDim));
+                    // One online log-sum-exp pass over the pieces; for each
+                    // piece the loads of every head are issued together.
+                    float Mr[kMaxG], Lr[kMaxG];
+                    float4 Ar[kMaxG];
+#pragma unroll
+                    for (int h = 0; h < kMaxG; ++h) {
+                        Mr[h] = NEG_INF;
+                        Lr[h] = 0.f;
+                        Ar[h] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+                    for (int i = i0; i <= i1; ++i) {
+                        const float* pi = p.partials + (static_cast<size_t>(i) * 2 + (i == i0 ? slot0 : 0)) * kPartialFloats;
+                        float mi[kMaxG], li[kMaxG];
+                        float4 oi[kMaxG];
+#pragma unroll
+                        for (int h = 0; h < kMaxG; ++h) {
+                            if (h < G) {
+                                mi[h] = __ldcg(pi + h * kORow + kDim);
+                                li[h] = __ldcg(pi + h * kORow + kDim + 1);
+                                oi[h] = __ldcg(reinterpret_cast<const float4*>(pi + h * kORow + d0));
+                            }
                         }
-                        float L = 0.f;
-                        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                        for (int i = i0; i <= i1; ++i) {
-                            const float* pi = p.partials +
-                                (static_cast<size_t>(i) * 2 + (i == i0 ? slot0 : 0)) * kPartialFloats + h * kORow;
-                            const float f = ex2(__ldcg(pi + kDim) - Mx);
-                            L += f * __ldcg(pi + kDim + 1);
-                            const float4 u = __ldcg(reinterpret_cast<const float4*>(pi + d0));
-                            acc.x += f * u.x; acc.y += f * u.y; acc.z += f * u.z; acc.w += f * u.w;
+#pragma unroll
+                        for (int h = 0; h < kMaxG; ++h) {
+                            if (h < G) {
+                                const float mn = fmaxf(Mr[h], mi[h]);
+                                const float a = ex2(Mr[h] - mn), b = ex2(mi[h] - mn);
+                                Lr[h] = Lr[h] * a + li[h] * b;
+                                Ar[h].x = Ar[h].x * a + oi[h].x * b;
+                                Ar[h].y = Ar[h].y * a + oi[h].y * b;
+                                Ar[h].z = Ar[h].z * a + oi[h].z * b;
+                                Ar[h].w = Ar[h].w * a + oi[h].w * b;
+                                Mr[h] = mn;
+                            }
                         }
-                        const float inv = 1.f / L;
-                        uint2 w2;
-                        w2.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-                        w2.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-                        *reinterpret_cast<uint2*>(out_base + static_cast<size_t>(h) * kDim) = w2;
+                    }
+#pragma unroll
+                    for (int h = 0; h < kMaxG; ++h) {
+                        if (h < G) {
+                            const float inv = 1.f / Lr[h];
+                            uint2 w2;
+                            w2.x = pack_bf16x2(Ar[h].x * inv, Ar[h].y * inv);
+                            w2.y = pack_bf16x2(Ar[h].z * inv, Ar[h].w * inv);
+                            *reinterpret_cast<uint2*>(out_base + static_cast<size_t>(h) * kDim) = w2;
+                        }
                     }
                     if (lane == 0) p.counters[s * Hkv + g] = 0;  // ready for the next launch
                 }
             }
             ++piece;
-            advance(cur, scan, B, Hkv, len);
-            x += len;
         }
         return;
     }
@@ -459,15 +526,13 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     const int v_sw = lane & 7;
     const float NEG_INF = -INFINITY;
 
-    Cursor cur = locate(scan, B, Hkv, range_lo);
-    long long x = range_lo;
+    PieceWalk walk(scan, B, Hkv, range_lo, range_hi);
+    Piece pc;
     long long gidx0 = 0;
     int qslot = 0, piece = 0;
     uint32_t qphase = 0;
-    while (x < range_hi) {
-        const int s = cur.s, blk0 = cur.blk;
-        const int nb = run_blocks(scan, s);
-        const int len = static_cast<int>(min(static_cast<long long>(nb - blk0), range_hi - x));
+    while (walk.next(pc)) {
+        const int s = pc.s, blk0 = pc.blk, nb = pc.nb, len = pc.len;
         const int ctx = clamped_ctx(p, s);
 
         // ---- query fragments (B operand of S^T = K Q^T) ----
@@ -593,8 +658,6 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         }
         mbar_arrive(mfull_bar(ms));
         ++piece;
-        advance(cur, scan, B, Hkv, len);
-        x += len;
     }
 }
 
