@@ -887,8 +887,13 @@ pkv_status pkv_decode_step(const void* k_new, const void* v_new, const int64_t* 
         if (st != PKV_OK) return st;
     }
     if (num_new_tokens > 0) {
-        st = pkv_append(k_new, v_new, slot_mapping, num_new_tokens, k_cache, v_cache, num_blocks, num_kv_heads,
-                        head_dim, device_error, stream);
+        // While the append runs, warm L2 with the attention's cold inputs.
+        const L2Warm warm = {{block_tables, q, context_lens},
+                             {static_cast<size_t>(num_seqs) * max_blocks_per_seq * 4,
+                              static_cast<size_t>(num_seqs) * num_q_heads * head_dim * 2,
+                              static_cast<size_t>(num_seqs) * 4}};
+        st = launch_append(k_new, v_new, slot_mapping, num_new_tokens, k_cache, v_cache, num_blocks, num_kv_heads,
+                           head_dim, device_error, stream, &warm);
         if (st != PKV_OK) return st;
     }
     return attn::launch(L, as_stream(stream), num_pairs > 0 || num_new_tokens > 0);

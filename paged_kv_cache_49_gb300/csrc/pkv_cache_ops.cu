@@ -12,6 +12,7 @@
 #include <algorithm>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 
 #include "pkv_internal.h"
 #include "pkv_ptx.cuh"
@@ -36,10 +37,17 @@ __global__ void __launch_bounds__(kThreads)
 append_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
               const int64_t* __restrict__ slots, long long rows, int hkv, int vec_per_row,
               long long slot_limit, uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
-              uint32_t* err) {
+              uint32_t* err, L2Warm warm) {
     griddep_launch_dependents();  // the attention of a decode step may start its prologue
     const long long per_tensor = rows * vec_per_row;
     const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+    const long long gtid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+#pragma unroll
+    for (int r = 0; r < 3; ++r) {
+        const char* base = static_cast<const char*>(warm.ptr[r]);
+        const long long lines = static_cast<long long>((warm.bytes[r] + 127) / 128);
+        for (long long l = gtid; base && l < lines; l += stride) prefetch_l2(base + l * 128);
+    }
     for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < 2 * per_tensor;
          i += stride) {
         const bool is_v = i >= per_tensor;
@@ -120,28 +128,59 @@ pkv_status pkv_read_device_error(uint32_t* device_error, uint32_t* host_value, i
     return PKV_OK;
 }
 
-pkv_status pkv_append(const void* k, const void* v, const int64_t* slot_mapping, int num_tokens,
-                      void* k_cache, void* v_cache, int num_blocks, int num_kv_heads, int head_dim,
-                      uint32_t* device_error, void* stream) {
+}  // extern "C"
+
+namespace pkv {
+
+// The decode-attention kernel runs with most of each SM's memory as shared
+// memory; giving the cache kernels the same preference spares the SMs a
+// reconfiguration between the kernels of a decode step.
+static void prefer_shared_carveout() {
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaFuncSetAttribute(ops::append_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+        cudaFuncSetAttribute(ops::copy_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+        cudaGetLastError();  // a refused preference is harmless
+    });
+}
+
+pkv_status launch_append(const void* k, const void* v, const int64_t* slot_mapping, int num_tokens,
+                         void* k_cache, void* v_cache, int num_blocks, int num_kv_heads, int head_dim,
+                         uint32_t* device_error, void* stream, const L2Warm* warm) {
     if (num_tokens < 0 || num_blocks < 1 || num_kv_heads < 1 || head_dim < 8 || head_dim % 8 != 0)
         return PKV_EINVAL;
     if (num_tokens == 0) return PKV_OK;
     if (!k || !v || !slot_mapping || !k_cache || !v_cache) return PKV_EINVAL;
     if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache)) return PKV_EINVAL;
+    prefer_shared_carveout();
     const int vec_per_row = head_dim / 8;
     const long long rows = static_cast<long long>(num_tokens) * num_kv_heads;
     const long long work = 2 * rows * vec_per_row;
     const int grid = static_cast<int>(std::min<long long>((work + ops::kThreads - 1) / ops::kThreads, 65535));
+    const L2Warm none = {{nullptr, nullptr, nullptr}, {0, 0, 0}};
     ops::append_kernel<<<grid, ops::kThreads, 0, as_stream(stream)>>>(
         static_cast<const uint4*>(k), static_cast<const uint4*>(v), slot_mapping, rows, num_kv_heads,
         vec_per_row, static_cast<long long>(num_blocks) * PKV_BLOCK_TOKENS, static_cast<uint4*>(k_cache),
-        static_cast<uint4*>(v_cache), device_error);
+        static_cast<uint4*>(v_cache), device_error, warm ? *warm : none);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         record_cuda_error(e);
         return PKV_ECUDA;
     }
     return PKV_OK;
+}
+
+}  // namespace pkv
+
+extern "C" {
+
+pkv_status pkv_append(const void* k, const void* v, const int64_t* slot_mapping, int num_tokens,
+                      void* k_cache, void* v_cache, int num_blocks, int num_kv_heads, int head_dim,
+                      uint32_t* device_error, void* stream) {
+    return launch_append(k, v, slot_mapping, num_tokens, k_cache, v_cache, num_blocks, num_kv_heads, head_dim,
+                         device_error, stream, nullptr);
 }
 
 pkv_status pkv_block_copy(void* k_cache, void* v_cache, const int32_t* src_dst_pairs, int num_pairs,
@@ -153,6 +192,7 @@ pkv_status pkv_block_copy(void* k_cache, void* v_cache, const int32_t* src_dst_p
     if (num_pairs > 65535) return PKV_ERANGE;
     if (!k_cache || !v_cache || !src_dst_pairs) return PKV_EINVAL;
     if (!aligned16(k_cache) || !aligned16(v_cache)) return PKV_EINVAL;
+    prefer_shared_carveout();
     const long long vec_per_block = static_cast<long long>(num_kv_heads) * PKV_BLOCK_TOKENS * head_dim / 8;
     const int gx = static_cast<int>(std::min<long long>((vec_per_block + ops::kThreads - 1) / ops::kThreads, 64));
     dim3 grid(gx, num_pairs, 2);

@@ -16,4 +16,16 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 inline cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 
+// Read-only inputs of a following kernel that the append kernel warms in L2
+// while it runs (used by pkv_decode_step for the attention's inputs).
+struct L2Warm {
+    const void* ptr[3];
+    size_t bytes[3];
+};
+
+// pkv_append's launch, optionally warming L2 with `warm` (may be null).
+pkv_status launch_append(const void* k, const void* v, const int64_t* slot_mapping, int num_tokens,
+                         void* k_cache, void* v_cache, int num_blocks, int num_kv_heads, int head_dim,
+                         uint32_t* device_error, void* stream, const L2Warm* warm);
+
 }  // namespace pkv
