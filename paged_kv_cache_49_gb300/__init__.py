@@ -13,3 +13,4 @@ from ._native import (  # noqa: F401
     read_device_error,
 )
 from .engine import PagedKVEngine, StepBuffers, bf16_from_bits, bits_from_bf16  # noqa: F401
+from .graphs import GraphedDecoder, default_buckets  # noqa: F401

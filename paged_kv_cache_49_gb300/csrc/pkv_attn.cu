@@ -45,7 +45,9 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <map>
 #include <mutex>
+#include <utility>
 #include <vector>
 
 #include "pkv_internal.h"
@@ -726,13 +728,26 @@ DeviceInfo device_info() {
 int grid_for(int num_seqs) {
     const DeviceInfo d = device_info();
     if (!d.ok) return 0;
+    // Cached per (device, shared memory size), so that a call made while a
+    // stream is being captured into a graph issues no CUDA query.
+    static std::mutex mu;
+    static std::map<std::pair<int, size_t>, int> cache;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const size_t smem = smem_bytes(num_seqs);
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto it = cache.find({dev, smem});
+        if (it != cache.end()) return it->second;
+    }
     int per_sm = 0;
-    const cudaError_t e =
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel, kThreads, smem_bytes(num_seqs));
+    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel, kThreads, smem);
     if (e != cudaSuccess || per_sm < 1) {
         record_cuda_error(e);
         return 0;
     }
+    std::lock_guard<std::mutex> lock(mu);
+    cache[{dev, smem}] = d.sm_count * per_sm;
     return d.sm_count * per_sm;
 }
 
