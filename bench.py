@@ -49,6 +49,7 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama3_8b_b64")
     ap.add_argument("--num-ctas", type=int, default=0)
+    ap.add_argument("--block-tokens", type=int, default=16, help="cache block size (8, 16, 32 or 64)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
@@ -61,13 +62,13 @@ def dist_info():
     return rank, world, local
 
 
-def algorithmic_bytes(ctx, hq, hkv, d=128):
+def algorithmic_bytes(ctx, hq, hkv, d=128, block_tokens=16):
     """Decode attention's bytes per launch: every context token's K and V
     rows once, q and out, the table entries read and the lengths."""
     ctx = np.asarray(ctx, dtype=np.int64)
     kv = int(ctx.sum()) * hkv * d * 2 * 2
     qo = 2 * len(ctx) * hq * d * 2
-    bt = int(((ctx + 15) // 16).sum()) * 4
+    bt = int(((ctx + block_tokens - 1) // block_tokens).sum()) * 4
     return kv + qo + bt + len(ctx) * 4
 
 
@@ -300,8 +301,10 @@ def run_ours(args):
     from workloads import make_workload
 
     # Weak scaling: every rank serves its own independent batch (seed = rank).
-    w = make_workload(args.workload, seed=rank)
-    eng = pkv.PagedKVEngine(w.pool_blocks, w.num_q_heads, w.num_kv_heads, w.head_dim, free_order=w.free_order)
+    extra = {} if args.block_tokens == 16 else {"block_tokens": args.block_tokens}
+    w = make_workload(args.workload, seed=rank, **extra)
+    eng = pkv.PagedKVEngine(w.pool_blocks, w.num_q_heads, w.num_kv_heads, w.head_dim, free_order=w.free_order,
+                            block_tokens=w.block_tokens)
     eng.load_workload_pool(w)
     eng.replay_events(w, with_content=True)
     q_bits, k_bits, v_bits = w.step_inputs()
@@ -390,13 +393,36 @@ def run_ours(args):
             e2e_ms = float(t.item())
         e2e = {"value": B * world / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+        # The same, with the step replayed from a CUDA graph (as a server does).
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            eng.run_step(sb, w.scale, args.num_ctas)
+        gts = []
+        for i in range(args.warmup + args.steps):
+            flush(i)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for name, t in host.items():
+                getattr(sb, name).copy_(t, non_blocking=True)
+            graph.replay()
+            out_host.copy_(sb.out, non_blocking=True)
+            e1.record(stream)
+            e1.synchronize()
+            if i >= args.warmup:
+                gts.append(e0.elapsed_time(e1))
+        g_ms = statistics.mean(gts)
+        if world > 1:
+            t = torch.tensor([g_ms], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            g_ms = float(t.item())
+        e2e["graph_replay"] = {"value": B * world / (g_ms * 1e-3), "ms_per_step": g_ms}
 
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
         return
 
-    abytes = algorithmic_bytes(ctx, w.num_q_heads, w.num_kv_heads)
+    abytes = algorithmic_bytes(ctx, w.num_q_heads, w.num_kv_heads, block_tokens=w.block_tokens)
     attn_s = statistics.mean(attn_ms) * 1e-3
     peak, peak_kind = measured_peak_gbs()
     achieved = abytes / attn_s / 1e9
@@ -413,7 +439,7 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "batch": B, "q_heads": w.num_q_heads, "kv_heads": w.num_kv_heads,
-                   "head_dim": w.head_dim, "block_tokens": 16, "context_tokens": int(ctx.sum()),
+                   "head_dim": w.head_dim, "block_tokens": w.block_tokens, "context_tokens": int(ctx.sum()),
                    "pool_blocks": w.pool_blocks, "cow_pairs_per_step": sb.num_pairs,
                    "num_ctas": args.num_ctas or pkv.default_ctas(B), "l2": "flushed before each timed launch (256 MiB write, then 256 MiB read: cold and clean)",
                    "parallelism": f"replicas x{world}"},

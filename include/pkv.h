@@ -101,6 +101,13 @@ pkv_status pkv_append(const void* k, const void* v, const int64_t* slot_mapping,
                       int num_kv_heads, int head_dim, uint32_t* device_error,
                       void* stream);
 
+/* pkv_append with a cache of block_tokens-token blocks (8, 16, 32 or 64):
+ * k_cache, v_cache are [num_blocks][num_kv_heads][block_tokens][head_dim] and
+ * slot = block * block_tokens + pos % block_tokens. */
+pkv_status pkv_append_ex(const void* k, const void* v, const int64_t* slot_mapping, int num_tokens,
+                         void* k_cache, void* v_cache, int num_blocks, int num_kv_heads, int head_dim,
+                         int block_tokens, uint32_t* device_error, void* stream);
+
 /*
  * pkv_block_copy -- copy-on-write of whole blocks.
  *
@@ -115,6 +122,11 @@ pkv_status pkv_append(const void* k, const void* v, const int64_t* slot_mapping,
 pkv_status pkv_block_copy(void* k_cache, void* v_cache, const int32_t* src_dst_pairs,
                           int num_pairs, int num_blocks, int num_kv_heads, int head_dim,
                           uint32_t* device_error, void* stream);
+
+/* pkv_block_copy for caches of block_tokens-token blocks (8, 16, 32 or 64). */
+pkv_status pkv_block_copy_ex(void* k_cache, void* v_cache, const int32_t* src_dst_pairs, int num_pairs,
+                             int num_blocks, int num_kv_heads, int head_dim, int block_tokens,
+                             uint32_t* device_error, void* stream);
 
 /*
  * pkv_attn_workspace_size -- bytes of device scratch pkv_attn_decode needs for
@@ -167,6 +179,22 @@ pkv_status pkv_attn_decode(const void* q, const void* k_cache, const void* v_cac
                            int num_kv_heads, int head_dim, int num_blocks, float scale,
                            int num_ctas, void* workspace, size_t workspace_bytes,
                            void* out, void* stream);
+
+/*
+ * pkv_attn_decode_ex -- pkv_attn_decode over a cache of block_tokens-token
+ * blocks (8, 16, 32 or 64; PKV_EUNSUPPORTED otherwise): token t of a sequence
+ * is row t % block_tokens of block table[t / block_tokens]. The block size
+ * trades tail waste and table length against the kernel's contiguous runs
+ * (cs2680 Lecture 10, §10.3, block-size table and Exercise 3: achieved
+ * attention bandwidth as a function of contiguous run length). A 128-dim
+ * head's block is block_tokens * 256 contiguous bytes; the kernel reads 16
+ * tokens at a time (two 8-token blocks when block_tokens is 8).
+ */
+pkv_status pkv_attn_decode_ex(const void* q, const void* k_cache, const void* v_cache,
+                              const int32_t* block_tables, int max_blocks_per_seq,
+                              const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads,
+                              int head_dim, int num_blocks, int block_tokens, float scale, int num_ctas,
+                              void* workspace, size_t workspace_bytes, void* out, void* stream);
 
 /*
  * pkv_decode_step -- one decode step of one attention layer in one call:
@@ -270,7 +298,8 @@ typedef struct pkv_bm_stats_t {
 } pkv_bm_stats_t;
 
 /* free_order: host int32 permutation of [0, num_blocks), or NULL. Returns NULL
- * on invalid arguments. block_tokens must be 16. */
+ * on invalid arguments. block_tokens: 8, 16, 32 or 64 (16 is the size the
+ * pages use and the one the other calls assume). */
 pkv_bm* pkv_bm_create(int num_blocks, int block_tokens, const int32_t* free_order);
 void pkv_bm_destroy(pkv_bm* bm);
 

@@ -38,8 +38,10 @@ EXPORTED = [
     "pkv_attn_decode", "pkv_attn_default_ctas", "pkv_bm_create", "pkv_bm_destroy",
     "pkv_bm_admit", "pkv_bm_fork", "pkv_bm_prepare_append", "pkv_bm_free",
     "pkv_bm_block_table", "pkv_bm_context_len", "pkv_bm_batch_tables", "pkv_bm_stats",
-    "pkv_bm_refcount", "pkv_attn_decode_static", "pkv_decode_step",
+    "pkv_bm_refcount", "pkv_attn_decode_static", "pkv_decode_step", "pkv_attn_decode_ex", "pkv_append_ex",
+    "pkv_block_copy_ex",
 ]
+BLOCK_SIZES = (8, 16, 32, 64)
 
 
 class PkvError(RuntimeError):
@@ -83,6 +85,9 @@ def _load() -> ctypes.CDLL:
         "pkv_read_device_error": (i32, [vp, vp, i32, vp]),
         "pkv_append": (i32, [vp, vp, vp, i32, vp, vp, i32, i32, i32, vp, vp]),
         "pkv_block_copy": (i32, [vp, vp, vp, i32, i32, i32, i32, vp, vp]),
+        "pkv_append_ex": (i32, [vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, vp, vp]),
+        "pkv_block_copy_ex": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, vp, vp]),
+        "pkv_attn_decode_ex": (i32, [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, f32, i32, vp, sz, vp, vp]),
         "pkv_attn_workspace_size": (sz, [i32, i32]),
         "pkv_attn_workspace_init": (i32, [vp, sz, vp]),
         "pkv_attn_decode": (i32, [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, f32, i32, vp, sz, vp, vp]),
@@ -169,13 +174,18 @@ def append(k, v, slot_mapping, k_cache, v_cache, device_error=None, stream=None)
     _need(k_cache, torch.bfloat16, "k_cache")
     _need(v_cache, torch.bfloat16, "v_cache")
     nb, hkv, bt, d = k_cache.shape
-    if v_cache.shape != k_cache.shape or bt != BLOCK_TOKENS:
-        raise ValueError("caches must be [num_blocks, Hkv, 16, D] and alike")
+    if v_cache.shape != k_cache.shape or bt not in BLOCK_SIZES:
+        raise ValueError("caches must be [num_blocks, Hkv, block_tokens in (8, 16, 32, 64), D] and alike")
     T = slot_mapping.numel()
     if k.shape != (T, hkv, d) or v.shape != (T, hkv, d):
         raise ValueError("k, v must be [T, Hkv, D] matching the cache and slot_mapping")
-    _check(_lib.pkv_append(_ptr(k), _ptr(v), _ptr(slot_mapping), T, _ptr(k_cache), _ptr(v_cache),
-                           nb, hkv, d, _ptr(device_error), _stream(stream)), "pkv_append")
+    if bt == BLOCK_TOKENS:
+        st = _lib.pkv_append(_ptr(k), _ptr(v), _ptr(slot_mapping), T, _ptr(k_cache), _ptr(v_cache),
+                             nb, hkv, d, _ptr(device_error), _stream(stream))
+    else:
+        st = _lib.pkv_append_ex(_ptr(k), _ptr(v), _ptr(slot_mapping), T, _ptr(k_cache), _ptr(v_cache),
+                                nb, hkv, d, bt, _ptr(device_error), _stream(stream))
+    _check(st, "pkv_append")
 
 
 def block_copy(k_cache, v_cache, pairs, device_error=None, stream=None) -> None:
@@ -187,8 +197,13 @@ def block_copy(k_cache, v_cache, pairs, device_error=None, stream=None) -> None:
     n = pairs.shape[0] if pairs.numel() else 0
     if n and pairs.shape != (n, 2):
         raise ValueError("pairs must be [n, 2]")
-    _check(_lib.pkv_block_copy(_ptr(k_cache), _ptr(v_cache), _ptr(pairs) if n else None, n, nb, hkv, d,
-                               _ptr(device_error), _stream(stream)), "pkv_block_copy")
+    if bt == BLOCK_TOKENS:
+        st = _lib.pkv_block_copy(_ptr(k_cache), _ptr(v_cache), _ptr(pairs) if n else None, n, nb, hkv, d,
+                                 _ptr(device_error), _stream(stream))
+    else:
+        st = _lib.pkv_block_copy_ex(_ptr(k_cache), _ptr(v_cache), _ptr(pairs) if n else None, n, nb, hkv, d, bt,
+                                    _ptr(device_error), _stream(stream))
+    _check(st, "pkv_block_copy")
 
 
 def default_ctas(num_seqs: int) -> int:
@@ -231,8 +246,8 @@ def attn_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out=None
     _need(context_lens, torch.int32, "context_lens")
     B, hq, d = q.shape
     nb, hkv, bt, d2 = k_cache.shape
-    if d != d2 or v_cache.shape != k_cache.shape or bt != BLOCK_TOKENS:
-        raise ValueError("q [B, Hq, D] and caches [NB, Hkv, 16, D] must agree")
+    if d != d2 or v_cache.shape != k_cache.shape or bt not in BLOCK_SIZES:
+        raise ValueError("q [B, Hq, D] and caches [NB, Hkv, block_tokens, D] must agree")
     if block_tables.dim() != 2 or block_tables.shape[0] != B or context_lens.shape != (B,):
         raise ValueError("block_tables must be [B, W] and context_lens [B]")
     if out is None:
@@ -240,10 +255,17 @@ def attn_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out=None
     _need(out, torch.bfloat16, "out")
     if workspace is None:
         workspace = AttentionWorkspace(B, hkv, device=q.device, stream=stream)
-    _check(_lib.pkv_attn_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
-                                block_tables.shape[1], _ptr(context_lens), B, hq, hkv, d, nb,
-                                float(scale), int(num_ctas), workspace.ptr, workspace.nbytes,
-                                _ptr(out), _stream(stream)), "pkv_attn_decode")
+    if bt == BLOCK_TOKENS:
+        st = _lib.pkv_attn_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                  block_tables.shape[1], _ptr(context_lens), B, hq, hkv, d, nb,
+                                  float(scale), int(num_ctas), workspace.ptr, workspace.nbytes,
+                                  _ptr(out), _stream(stream))
+    else:
+        st = _lib.pkv_attn_decode_ex(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                     block_tables.shape[1], _ptr(context_lens), B, hq, hkv, d, nb, bt,
+                                     float(scale), int(num_ctas), workspace.ptr, workspace.nbytes,
+                                     _ptr(out), _stream(stream))
+    _check(st, "pkv_attn_decode")
     return out
 
 

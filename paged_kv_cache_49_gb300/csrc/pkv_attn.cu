@@ -56,7 +56,7 @@
 namespace pkv {
 namespace attn {
 
-constexpr int kTok = PKV_BLOCK_TOKENS;   // tokens per block
+constexpr int kTok = 16;  // tokens per tile, the kernel's unit of work (cache blocks hold kBT tokens)
 constexpr int kDim = PKV_ATTN_HEAD_DIM;  // head dim
 constexpr int kMaxG = PKV_ATTN_MAX_GROUP;
 constexpr int kConsumerWarps = 4;
@@ -109,6 +109,7 @@ struct Params {
     int num_kv_heads;
     int group;
     int max_blocks;
+    int cap_tokens;  // max_blocks * block tokens: longest context a table row can hold
     int num_blocks;
     float scale_log2;
     uint32_t* err;
@@ -157,10 +158,8 @@ __device__ __forceinline__ void advance(Cursor& c, const int* scan, int n, int h
 }
 
 __device__ __forceinline__ int clamped_ctx(const Params& p, int s) {
-    int c = __ldg(p.context_lens + s);
-    const int cap = p.max_blocks * kTok;
-    if (c > cap) c = cap;
-    return c;
+    const int c = __ldg(p.context_lens + s);
+    return c > p.cap_tokens ? p.cap_tokens : c;
 }
 
 // One piece: blocks [blk, blk + len) of the run of (sequence s, KV head g),
@@ -214,6 +213,10 @@ struct PieceWalk {
     }
 };
 
+// kBT: tokens per cache block (8, 16, 32 or 64). A 16-token tile is rows
+// [(t mod kBT/16) * 16, +16) of block table[t / (kBT/16)] when kBT >= 16, and
+// the two 8-row blocks table[2t], table[2t + 1] when kBT == 8.
+template <int kBT>
 __global__ void __launch_bounds__(kThreads, 2)
 decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
               const Params p) {
@@ -267,7 +270,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         const int per = (B + kThreads - 1) / kThreads;
         const int lo = min(B, tid * per);
         const int hi = min(B, lo + per);
-        const int cap = p.max_blocks * kTok;
+        const int cap = p.cap_tokens;
         int local = 0;
         for (int s = lo; s < hi; ++s) {
             const int c = __ldg(p.context_lens + s);
@@ -306,8 +309,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         for (long long xx = range_lo; xx < range_hi;) {
             const int nb = run_blocks(scan, c.s);
             const int len = static_cast<int>(min(static_cast<long long>(nb - c.blk), range_hi - xx));
-            const int32_t* t0 = p.block_tables + static_cast<size_t>(c.s) * p.max_blocks + c.blk;
-            const char* t1 = reinterpret_cast<const char*>(t0 + len);
+            const int e0 = c.blk * kTok / kBT, e1 = ((c.blk + len) * kTok + kBT - 1) / kBT;
+            const int32_t* t0 = p.block_tables + static_cast<size_t>(c.s) * p.max_blocks + e0;
+            const char* t1 = reinterpret_cast<const char*>(t0 + (e1 - e0));
             const char* line = reinterpret_cast<const char*>(reinterpret_cast<uintptr_t>(t0) & ~uintptr_t(127));
             for (const char* a = line + lane * 128; a < t1; a += 32 * 128) prefetch_l2(a);
             const char* qrow = reinterpret_cast<const char*>(
@@ -355,29 +359,54 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 }
             }
             if (++qslot == kQSlots) { qslot = 0; qphase ^= 1u; }
-            const int32_t* row = p.block_tables + static_cast<size_t>(pc.s) * p.max_blocks + pc.blk;
+            const int32_t* row = p.block_tables + static_cast<size_t>(pc.s) * p.max_blocks;
+            const int seq_blocks = (clamped_ctx(p, pc.s) + kBT - 1) / kBT;  // valid table entries
+            auto block_id = [&](int e) {
+                int bid = __ldg(row + e);
+                if (bid < 0 || bid >= p.num_blocks) {
+                    if (p.err) atomicOr(p.err, PKV_DEVERR_BLOCK_ID);
+                    bid = 0;  // read a valid block instead; the output is flagged invalid
+                }
+                return bid;
+            };
             for (int j0 = 0; j0 < len; j0 += 32) {
-                int bid = 0;
+                int y0 = 0, y1 = 0;  // token-row coordinates of the tile's rows 0 and 8
                 if (j0 + lane < len) {
-                    bid = __ldg(row + j0 + lane);
-                    if (bid < 0 || bid >= p.num_blocks) {
-                        if (p.err) atomicOr(p.err, PKV_DEVERR_BLOCK_ID);
-                        bid = 0;  // read a valid block instead; the output is flagged invalid
+                    const int t = pc.blk + j0 + lane;  // tile index within the sequence
+                    if constexpr (kBT >= kTok) {
+                        y0 = (block_id(t / (kBT / kTok)) * Hkv + pc.g) * kBT + (t % (kBT / kTok)) * kTok;
+                    } else {
+                        const int b0 = block_id(2 * t);
+                        const int b1 = 2 * t + 1 < seq_blocks ? block_id(2 * t + 1) : b0;  // past the end: masked
+                        y0 = (b0 * Hkv + pc.g) * kBT;
+                        y1 = (b1 * Hkv + pc.g) * kBT;
                     }
                 }
                 const int n = min(32, len - j0);
                 for (int jj = 0; jj < n; ++jj) {
-                    const int b = __shfl_sync(0xffffffffu, bid, jj);
+                    const int ya = __shfl_sync(0xffffffffu, y0, jj);
+                    const int yb = __shfl_sync(0xffffffffu, y1, jj);
                     if (lane == 0) {
                         if (mbar_wait(empty_bar(stage), sphase ^ 1u, abort_flag, p.err)) {
                             const uint32_t fb = full_bar(stage);
                             mbar_arrive_expect_tx(fb, kStageBytes);
-                            const int y = (b * Hkv + pc.g) * kTok;
                             const uint32_t dst = smem_u32(smem + kOffStages + stage * kStageBytes);
-                            tma_load_2d(dst, &tm_k, 0, y, fb, policy);
-                            tma_load_2d(dst + kHalfBytes, &tm_k, 64, y, fb, policy);
-                            tma_load_2d(dst + kBlockBytes, &tm_v, 0, y, fb, policy);
-                            tma_load_2d(dst + kBlockBytes + kHalfBytes, &tm_v, 64, y, fb, policy);
+                            if constexpr (kBT >= kTok) {
+                                tma_load_2d(dst, &tm_k, 0, ya, fb, policy);
+                                tma_load_2d(dst + kHalfBytes, &tm_k, 64, ya, fb, policy);
+                                tma_load_2d(dst + kBlockBytes, &tm_v, 0, ya, fb, policy);
+                                tma_load_2d(dst + kBlockBytes + kHalfBytes, &tm_v, 64, ya, fb, policy);
+                            } else {  // 8-row boxes: rows 0-7 from one block, rows 8-15 from the next
+                                constexpr uint32_t kRow8 = 8 * 128;
+                                tma_load_2d(dst, &tm_k, 0, ya, fb, policy);
+                                tma_load_2d(dst + kRow8, &tm_k, 0, yb, fb, policy);
+                                tma_load_2d(dst + kHalfBytes, &tm_k, 64, ya, fb, policy);
+                                tma_load_2d(dst + kHalfBytes + kRow8, &tm_k, 64, yb, fb, policy);
+                                tma_load_2d(dst + kBlockBytes, &tm_v, 0, ya, fb, policy);
+                                tma_load_2d(dst + kBlockBytes + kRow8, &tm_v, 0, yb, fb, policy);
+                                tma_load_2d(dst + kBlockBytes + kHalfBytes, &tm_v, 64, ya, fb, policy);
+                                tma_load_2d(dst + kBlockBytes + kHalfBytes + kRow8, &tm_v, 64, yb, fb, policy);
+                            }
                             ++issued;
                         }
                     }
@@ -682,18 +711,32 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// 2-D view of a cache: rows = num_blocks * Hkv * 16 token rows of 128 bf16.
-bool make_cache_map(CUtensorMap* map, const void* base, int num_blocks, int hkv) {
+// 2-D view of a cache: rows = num_blocks * Hkv * block_tokens token rows of
+// 128 bf16; a box is 64 columns by min(16, block_tokens) rows.
+bool make_cache_map(CUtensorMap* map, const void* base, int num_blocks, int hkv, int block_tokens) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(kDim),
-                          static_cast<cuuint64_t>(num_blocks) * hkv * kTok};
+                          static_cast<cuuint64_t>(num_blocks) * hkv * block_tokens};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(kDim) * 2};
-    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kTok)};
+    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(block_tokens < kTok ? block_tokens : kTok)};
     cuuint32_t estr[2] = {1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+using KernelFn = void (*)(CUtensorMap, CUtensorMap, Params);
+
+// The instantiation for a block size (8, 16, 32 or 64 tokens), else null.
+KernelFn kernel_for(int block_tokens) {
+    switch (block_tokens) {
+        case 8: return decode_kernel<8>;
+        case 16: return decode_kernel<16>;
+        case 32: return decode_kernel<32>;
+        case 64: return decode_kernel<64>;
+        default: return nullptr;
+    }
 }
 
 struct DeviceInfo {
@@ -711,8 +754,11 @@ DeviceInfo device_info() {
     if (static_cast<int>(cache.size()) <= dev) cache.resize(dev + 1);
     DeviceInfo& d = cache[dev];
     if (d.ok) return d;
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem_bytes(PKV_ATTN_MAX_SEQS)));
+    cudaError_t e = cudaSuccess;
+    for (int bt : {8, 16, 32, 64})
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(kernel_for(bt), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(smem_bytes(PKV_ATTN_MAX_SEQS)));
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) {
         record_cuda_error(e);
@@ -725,29 +771,31 @@ DeviceInfo device_info() {
 // Persistent CTAs for a batch of num_seqs: every CTA that fits at once (the
 // shared-memory prefix sum grows with num_seqs, so large batches may fit one
 // CTA per SM instead of two). 0 on error.
-int grid_for(int num_seqs) {
+int grid_for(int num_seqs, int block_tokens = PKV_BLOCK_TOKENS) {
     const DeviceInfo d = device_info();
-    if (!d.ok) return 0;
-    // Cached per (device, shared memory size), so that a call made while a
-    // stream is being captured into a graph issues no CUDA query.
+    const KernelFn fn = kernel_for(block_tokens);
+    if (!d.ok || !fn) return 0;
+    // Cached per (device, block size, shared memory size), so that a call
+    // made while a stream is being captured into a graph issues no CUDA query.
     static std::mutex mu;
     static std::map<std::pair<int, size_t>, int> cache;
     int dev = 0;
     cudaGetDevice(&dev);
     const size_t smem = smem_bytes(num_seqs);
+    const std::pair<int, size_t> key{dev * 128 + block_tokens, smem};
     {
         std::lock_guard<std::mutex> lock(mu);
-        auto it = cache.find({dev, smem});
+        auto it = cache.find(key);
         if (it != cache.end()) return it->second;
     }
     int per_sm = 0;
-    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel, kThreads, smem);
+    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, smem);
     if (e != cudaSuccess || per_sm < 1) {
         record_cuda_error(e);
         return 0;
     }
     std::lock_guard<std::mutex> lock(mu);
-    cache[{dev, smem}] = d.sm_count * per_sm;
+    cache[key] = d.sm_count * per_sm;
     return d.sm_count * per_sm;
 }
 
@@ -756,13 +804,16 @@ struct Launch {
     Params prm;
     int grid;
     size_t smem;
+    KernelFn fn;
 };
 
 // Validate pkv_attn_decode's arguments and build its launch.
 pkv_status prepare(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
                    int max_blocks_per_seq, const int32_t* context_lens, int num_seqs, int num_q_heads,
                    int num_kv_heads, int head_dim, int num_blocks, float scale, int num_ctas, void* workspace,
-                   size_t workspace_bytes, void* out, Launch* L) {
+                   size_t workspace_bytes, void* out, Launch* L, int block_tokens = PKV_BLOCK_TOKENS) {
+    L->fn = kernel_for(block_tokens);
+    if (!L->fn) return PKV_EUNSUPPORTED;
     if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !workspace || !out)
         return PKV_EINVAL;
     if (num_seqs < 1 || num_q_heads < 1 || num_kv_heads < 1 || num_blocks < 1 ||
@@ -771,15 +822,15 @@ pkv_status prepare(const void* q, const void* k_cache, const void* v_cache, cons
     if (num_seqs > PKV_ATTN_MAX_SEQS || head_dim != PKV_ATTN_HEAD_DIM ||
         num_q_heads % num_kv_heads != 0 || num_q_heads / num_kv_heads > PKV_ATTN_MAX_GROUP)
         return PKV_EUNSUPPORTED;
-    if (static_cast<long long>(num_blocks) * num_kv_heads * PKV_BLOCK_TOKENS >= (1ll << 31) ||
+    if (static_cast<long long>(num_blocks) * num_kv_heads * block_tokens >= (1ll << 31) ||
         static_cast<long long>(num_seqs) * max_blocks_per_seq >= (1ll << 31) ||
-        static_cast<long long>(max_blocks_per_seq) * PKV_BLOCK_TOKENS >= (1ll << 31) ||
-        static_cast<long long>(num_kv_heads) * num_seqs * max_blocks_per_seq >= (1ll << 31))
+        static_cast<long long>(max_blocks_per_seq) * block_tokens >= (1ll << 31) ||
+        static_cast<long long>(num_kv_heads) * num_seqs * max_blocks_per_seq * block_tokens / kTok >= (1ll << 31))
         return PKV_ERANGE;
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
         (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
         return PKV_EINVAL;
-    const int auto_grid = grid_for(num_seqs);
+    const int auto_grid = grid_for(num_seqs, block_tokens);
     if (auto_grid < 1) return PKV_ECUDA;
     int grid = num_ctas > 0 ? num_ctas : auto_grid;
     const size_t fixed = kWsHeader + align256(static_cast<size_t>(num_seqs) * num_kv_heads * 4);
@@ -789,8 +840,8 @@ pkv_status prepare(const void* q, const void* k_cache, const void* v_cache, cons
         if (num_ctas > 0) return PKV_EINVAL;
         grid = static_cast<int>(fit);
     }
-    if (!make_cache_map(&L->tm_k, k_cache, num_blocks, num_kv_heads) ||
-        !make_cache_map(&L->tm_v, v_cache, num_blocks, num_kv_heads))
+    if (!make_cache_map(&L->tm_k, k_cache, num_blocks, num_kv_heads, block_tokens) ||
+        !make_cache_map(&L->tm_v, v_cache, num_blocks, num_kv_heads, block_tokens))
         return PKV_ECUDA;
     Params& prm = L->prm;
     prm.q = static_cast<const __nv_bfloat16*>(q);
@@ -802,6 +853,7 @@ pkv_status prepare(const void* q, const void* k_cache, const void* v_cache, cons
     prm.num_kv_heads = num_kv_heads;
     prm.group = num_q_heads / num_kv_heads;
     prm.max_blocks = max_blocks_per_seq;
+    prm.cap_tokens = max_blocks_per_seq * block_tokens;
     prm.num_blocks = num_blocks;
     prm.scale_log2 = scale * 1.4426950408889634f;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -826,7 +878,7 @@ pkv_status launch(const Launch& L, cudaStream_t stream, bool early) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = early ? 1 : 0;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, decode_kernel, L.tm_k, L.tm_v, L.prm);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, L.fn, L.tm_k, L.tm_v, L.prm);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) {
         record_cuda_error(e);
@@ -878,6 +930,19 @@ pkv_status pkv_attn_decode(const void* q, const void* k_cache, const void* v_cac
     return attn::launch(L, as_stream(stream), false);
 }
 
+pkv_status pkv_attn_decode_ex(const void* q, const void* k_cache, const void* v_cache,
+                              const int32_t* block_tables, int max_blocks_per_seq,
+                              const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads,
+                              int head_dim, int num_blocks, int block_tokens, float scale, int num_ctas,
+                              void* workspace, size_t workspace_bytes, void* out, void* stream) {
+    attn::Launch L;
+    const pkv_status st = attn::prepare(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                                        num_seqs, num_q_heads, num_kv_heads, head_dim, num_blocks, scale,
+                                        num_ctas, workspace, workspace_bytes, out, &L, block_tokens);
+    if (st != PKV_OK) return st;
+    return attn::launch(L, as_stream(stream), false);
+}
+
 pkv_status pkv_decode_step(const void* k_new, const void* v_new, const int64_t* slot_mapping,
                            int num_new_tokens, const int32_t* src_dst_pairs, int num_pairs,
                            void* k_cache, void* v_cache, int num_blocks, const void* q,
@@ -908,7 +973,7 @@ pkv_status pkv_decode_step(const void* k_new, const void* v_new, const int64_t* 
                               static_cast<size_t>(num_seqs) * num_q_heads * head_dim * 2,
                               static_cast<size_t>(num_seqs) * 4}};
         st = launch_append(k_new, v_new, slot_mapping, num_new_tokens, k_cache, v_cache, num_blocks, num_kv_heads,
-                           head_dim, device_error, stream, &warm);
+                           head_dim, PKV_BLOCK_TOKENS, device_error, stream, &warm);
         if (st != PKV_OK) return st;
     }
     return attn::launch(L, as_stream(stream), num_pairs > 0 || num_new_tokens > 0);
@@ -992,8 +1057,8 @@ extern "C" pkv_status pkv_attn_decode_static(const void* q, const void* k_cache,
     const int grid = auto_grid < attn::kStaticMaxCtas ? auto_grid : attn::kStaticMaxCtas;
 
     CUtensorMap tm_k, tm_v;
-    if (!attn::make_cache_map(&tm_k, k_cache, num_blocks, num_kv_heads) ||
-        !attn::make_cache_map(&tm_v, v_cache, num_blocks, num_kv_heads))
+    if (!attn::make_cache_map(&tm_k, k_cache, num_blocks, num_kv_heads, PKV_BLOCK_TOKENS) ||
+        !attn::make_cache_map(&tm_v, v_cache, num_blocks, num_kv_heads, PKV_BLOCK_TOKENS))
         return PKV_ECUDA;
 
     // The counters must start at zero; a previous call leaves them at zero
@@ -1016,13 +1081,15 @@ extern "C" pkv_status pkv_attn_decode_static(const void* q, const void* k_cache,
     prm.num_kv_heads = num_kv_heads;
     prm.group = num_q_heads / num_kv_heads;
     prm.max_blocks = max_blocks_per_seq;
+    prm.cap_tokens = max_blocks_per_seq * PKV_BLOCK_TOKENS;
     prm.num_blocks = num_blocks;
     prm.scale_log2 = scale * 1.4426950408889634f;
     prm.err = device_error ? device_error : reinterpret_cast<uint32_t*>(scratch);
     prm.counters = reinterpret_cast<int*>(scratch + attn::kWsHeader);
     prm.partials = reinterpret_cast<float*>(scratch + attn::kWsHeader + attn::kStaticCounterBytes);
 
-    attn::decode_kernel<<<grid, attn::kThreads, attn::smem_bytes(num_seqs), as_stream(stream)>>>(tm_k, tm_v, prm);
+    attn::decode_kernel<PKV_BLOCK_TOKENS>
+        <<<grid, attn::kThreads, attn::smem_bytes(num_seqs), as_stream(stream)>>>(tm_k, tm_v, prm);
     e = cudaGetLastError();
     if (e != cudaSuccess) {
         record_cuda_error(e);

@@ -58,7 +58,8 @@ struct pkv_bm {
 extern "C" {
 
 pkv_bm* pkv_bm_create(int num_blocks, int block_tokens, const int32_t* free_order) {
-    if (num_blocks <= 0 || block_tokens != PKV_BLOCK_TOKENS) return nullptr;
+    if (num_blocks <= 0 || (block_tokens != 8 && block_tokens != 16 && block_tokens != 32 && block_tokens != 64))
+        return nullptr;
     auto* bm = new pkv_bm();
     bm->num_blocks = num_blocks;
     bm->block_tokens = block_tokens;

@@ -35,7 +35,7 @@ constexpr int kThreads = 256;
 // vec_per_row = head_dim / 8.
 __global__ void __launch_bounds__(kThreads)
 append_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
-              const int64_t* __restrict__ slots, long long rows, int hkv, int vec_per_row,
+              const int64_t* __restrict__ slots, long long rows, int hkv, int vec_per_row, int bt,
               long long slot_limit, uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
               uint32_t* err, L2Warm warm) {
     griddep_launch_dependents();  // the attention of a decode step may start its prologue
@@ -62,9 +62,9 @@ append_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
             if (err && vec == 0 && head == 0 && !is_v) atomicOr(err, PKV_DEVERR_SLOT);
             continue;
         }
-        const long long blk = slot >> 4;
-        const long long pos = slot & 15;
-        const long long dst = ((blk * hkv + head) * 16 + pos) * vec_per_row + vec;
+        const long long blk = slot / bt;
+        const long long pos = slot - blk * bt;
+        const long long dst = ((blk * hkv + head) * bt + pos) * vec_per_row + vec;
         if (is_v) v_cache[dst] = __ldg(v + j);
         else k_cache[dst] = __ldg(k + j);
     }
@@ -148,8 +148,9 @@ static void prefer_shared_carveout() {
 
 pkv_status launch_append(const void* k, const void* v, const int64_t* slot_mapping, int num_tokens,
                          void* k_cache, void* v_cache, int num_blocks, int num_kv_heads, int head_dim,
-                         uint32_t* device_error, void* stream, const L2Warm* warm) {
-    if (num_tokens < 0 || num_blocks < 1 || num_kv_heads < 1 || head_dim < 8 || head_dim % 8 != 0)
+                         int block_tokens, uint32_t* device_error, void* stream, const L2Warm* warm) {
+    if (num_tokens < 0 || num_blocks < 1 || num_kv_heads < 1 || head_dim < 8 || head_dim % 8 != 0 ||
+        block_tokens < 1)
         return PKV_EINVAL;
     if (num_tokens == 0) return PKV_OK;
     if (!k || !v || !slot_mapping || !k_cache || !v_cache) return PKV_EINVAL;
@@ -162,7 +163,7 @@ pkv_status launch_append(const void* k, const void* v, const int64_t* slot_mappi
     const L2Warm none = {{nullptr, nullptr, nullptr}, {0, 0, 0}};
     ops::append_kernel<<<grid, ops::kThreads, 0, as_stream(stream)>>>(
         static_cast<const uint4*>(k), static_cast<const uint4*>(v), slot_mapping, rows, num_kv_heads,
-        vec_per_row, static_cast<long long>(num_blocks) * PKV_BLOCK_TOKENS, static_cast<uint4*>(k_cache),
+        vec_per_row, block_tokens, static_cast<long long>(num_blocks) * block_tokens, static_cast<uint4*>(k_cache),
         static_cast<uint4*>(v_cache), device_error, warm ? *warm : none);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
@@ -180,20 +181,35 @@ pkv_status pkv_append(const void* k, const void* v, const int64_t* slot_mapping,
                       void* k_cache, void* v_cache, int num_blocks, int num_kv_heads, int head_dim,
                       uint32_t* device_error, void* stream) {
     return launch_append(k, v, slot_mapping, num_tokens, k_cache, v_cache, num_blocks, num_kv_heads, head_dim,
-                         device_error, stream, nullptr);
+                         PKV_BLOCK_TOKENS, device_error, stream, nullptr);
+}
+
+pkv_status pkv_append_ex(const void* k, const void* v, const int64_t* slot_mapping, int num_tokens,
+                         void* k_cache, void* v_cache, int num_blocks, int num_kv_heads, int head_dim,
+                         int block_tokens, uint32_t* device_error, void* stream) {
+    return launch_append(k, v, slot_mapping, num_tokens, k_cache, v_cache, num_blocks, num_kv_heads, head_dim,
+                         block_tokens, device_error, stream, nullptr);
 }
 
 pkv_status pkv_block_copy(void* k_cache, void* v_cache, const int32_t* src_dst_pairs, int num_pairs,
                           int num_blocks, int num_kv_heads, int head_dim, uint32_t* device_error,
                           void* stream) {
-    if (num_pairs < 0 || num_blocks < 1 || num_kv_heads < 1 || head_dim < 8 || head_dim % 8 != 0)
+    return pkv_block_copy_ex(k_cache, v_cache, src_dst_pairs, num_pairs, num_blocks, num_kv_heads, head_dim,
+                             PKV_BLOCK_TOKENS, device_error, stream);
+}
+
+pkv_status pkv_block_copy_ex(void* k_cache, void* v_cache, const int32_t* src_dst_pairs, int num_pairs,
+                             int num_blocks, int num_kv_heads, int head_dim, int block_tokens,
+                             uint32_t* device_error, void* stream) {
+    if (num_pairs < 0 || num_blocks < 1 || num_kv_heads < 1 || head_dim < 8 || head_dim % 8 != 0 ||
+        block_tokens < 1)
         return PKV_EINVAL;
     if (num_pairs == 0) return PKV_OK;
     if (num_pairs > 65535) return PKV_ERANGE;
     if (!k_cache || !v_cache || !src_dst_pairs) return PKV_EINVAL;
     if (!aligned16(k_cache) || !aligned16(v_cache)) return PKV_EINVAL;
     prefer_shared_carveout();
-    const long long vec_per_block = static_cast<long long>(num_kv_heads) * PKV_BLOCK_TOKENS * head_dim / 8;
+    const long long vec_per_block = static_cast<long long>(num_kv_heads) * block_tokens * head_dim / 8;
     const int gx = static_cast<int>(std::min<long long>((vec_per_block + ops::kThreads - 1) / ops::kThreads, 64));
     dim3 grid(gx, num_pairs, 2);
     ops::copy_kernel<<<grid, ops::kThreads, 0, as_stream(stream)>>>(

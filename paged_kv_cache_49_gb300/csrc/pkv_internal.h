@@ -26,6 +26,6 @@ struct L2Warm {
 // pkv_append's launch, optionally warming L2 with `warm` (may be null).
 pkv_status launch_append(const void* k, const void* v, const int64_t* slot_mapping, int num_tokens,
                          void* k_cache, void* v_cache, int num_blocks, int num_kv_heads, int head_dim,
-                         uint32_t* device_error, void* stream, const L2Warm* warm);
+                         int block_tokens, uint32_t* device_error, void* stream, const L2Warm* warm);
 
 }  // namespace pkv

@@ -48,14 +48,15 @@ class StepBuffers:
 
 class PagedKVEngine:
     def __init__(self, num_blocks: int, num_q_heads: int, num_kv_heads: int, head_dim: int = 128,
-                 device="cuda", free_order=None):
+                 device="cuda", free_order=None, block_tokens: int = nat.BLOCK_TOKENS):
         self.num_blocks, self.num_q_heads, self.num_kv_heads, self.head_dim = (
             num_blocks, num_q_heads, num_kv_heads, head_dim)
+        self.block_tokens = block_tokens
         self.device = torch.device(device)
-        shape = (num_blocks, num_kv_heads, nat.BLOCK_TOKENS, head_dim)
+        shape = (num_blocks, num_kv_heads, block_tokens, head_dim)
         self.k_cache = torch.empty(shape, dtype=torch.bfloat16, device=self.device)
         self.v_cache = torch.empty(shape, dtype=torch.bfloat16, device=self.device)
-        self.bm = nat.BlockManager(num_blocks, nat.BLOCK_TOKENS, free_order)
+        self.bm = nat.BlockManager(num_blocks, block_tokens, free_order)
         self.error = nat.new_error_word(self.device)
 
     # ---- pool content ----------------------------------------------------
@@ -128,7 +129,10 @@ class PagedKVEngine:
 
     def run_step(self, sb: StepBuffers, scale: float, num_ctas: int = 0, stream=None) -> torch.Tensor:
         """The device part of a decode step -- copy-on-write copies, append,
-        attention -- as one library call. Idempotent for fixed inputs."""
+        attention -- as one library call (separate calls for block sizes
+        other than 16). Idempotent for fixed inputs."""
+        if self.block_tokens != nat.BLOCK_TOKENS:
+            return self.run_step_separate(sb, scale, num_ctas, stream)
         return nat.decode_step(sb.q, sb.k, sb.v, sb.slots, sb.pairs, self.k_cache, self.v_cache, sb.tables,
                                sb.ctx, scale, sb.out, sb.workspace, self.error, num_ctas, stream)
 

@@ -57,4 +57,8 @@ def test_host_argument_checks_need_no_gpu(lib_path):
     assert L.pkv_block_copy(None, None, None, 3, 1, 8, 127, None, None) == nat.PKV_EINVAL
     assert L.pkv_attn_workspace_size(0, 8) == 0
     assert L.pkv_bm_create(0, 16, None) is None
-    assert L.pkv_bm_create(4, 8, None) is None
+    assert L.pkv_bm_create(4, 12, None) is None  # block sizes are 8, 16, 32 or 64
+    h = L.pkv_bm_create(4, 8, None)
+    assert h is not None
+    L.pkv_bm_destroy(h)
+    assert L.pkv_attn_decode_ex(None, None, None, None, 1, None, 1, 32, 8, 128, 1, 16, 1.0, 0, None, 0, None, None) == nat.PKV_EINVAL

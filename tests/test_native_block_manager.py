@@ -76,19 +76,20 @@ def _same_state(o, n, ids):
 
 
 @pytest.mark.parametrize("seed", range(12))
-def test_random_operations_match_oracle(nat, seed):
+@pytest.mark.parametrize("bt", [16, 8, 32, 64])
+def test_random_operations_match_oracle(nat, seed, bt):
     rnd = random.Random(seed)
-    nb = rnd.randint(16, 160)
+    nb = rnd.randint(16, 160) * 16 // bt
     order = rnd.sample(range(nb), nb) if seed % 2 else None
-    o = obm.BlockManager(nb, 16, order)
-    n = nat.BlockManager(nb, 16, order)
+    o = obm.BlockManager(nb, bt, order)
+    n = nat.BlockManager(nb, bt, order)
     for _ in range(250):
         live = sorted(o.seqs)
         op = rnd.random()
         if op < 0.3 or not live:
             grp = rnd.choice([-1, -1, 0, 1])
             p = rnd.randint(0, 60)
-            args = (p, rnd.randint(0, 40), grp, 16 * rnd.randint(0, p // 16) if grp >= 0 else 0)
+            args = (p, rnd.randint(0, 40), grp, bt * rnd.randint(0, p // bt) if grp >= 0 else 0)
             _both(nat, lambda: o.admit(*args), lambda: n.admit(*args))
         elif op < 0.45:
             par, k = rnd.choice(live), rnd.randint(0, 3)

@@ -160,28 +160,29 @@ def _lognormal_lengths(rng, n, median, sigma, lo, hi):
     return np.clip(np.rint(x), lo, hi).astype(np.int64)
 
 
-def _pool_bound(token_counts, slack=1.1):
+def _pool_bound(token_counts, slack=1.1, block_tokens=BLOCK_TOKENS):
     """Pool size (blocks) comfortably above the pages the requests reserve."""
     tokens = int(np.sum(token_counts))
-    return int(math.ceil(slack * (tokens / BLOCK_TOKENS + len(token_counts))))
+    return int(math.ceil(slack * (tokens / block_tokens + len(token_counts))))
 
 
-def _decode_batch(name, desc, seed, hq, hkv, ctx, pool_blocks=None, fill="randn"):
+def _decode_batch(name, desc, seed, hq, hkv, ctx, pool_blocks=None, fill="randn", block_tokens=BLOCK_TOKENS):
     """Every sequence holds ctx-1 tokens and appends its ctx-th in the step."""
     ctx = [int(c) for c in ctx]
     events = [("admit", c - 1, 1, -1, 0) for c in ctx]
     if pool_blocks is None:
-        pool_blocks = _pool_bound(ctx)
-    w = Workload(name, desc, seed, hq, hkv, 128, pool_blocks, events, list(range(len(ctx))))
+        pool_blocks = _pool_bound(ctx, block_tokens=block_tokens)
+    w = Workload(name, desc, seed, hq, hkv, 128, pool_blocks, events, list(range(len(ctx))),
+                 block_tokens=block_tokens)
     w.free_order = _rng(seed, _TAG_PARAMS, 1).permutation(pool_blocks).astype(np.int32)
     w.pool_fill = fill
     return w
 
 
-def tiny(seed: int = 0) -> Workload:
+def tiny(seed: int = 0, block_tokens: int = BLOCK_TOKENS) -> Workload:
     return _decode_batch(
         "tiny", "batch 4, ctx {1,16,17,203}, 32 q / 8 kv heads, d_h 128, 64-block permuted pool",
-        seed, 32, 8, [1, 16, 17, 203], pool_blocks=64)
+        seed, 32, 8, [1, 16, 17, 203], pool_blocks=64, block_tokens=block_tokens)
 
 
 def tiny_nan(seed: int = 0) -> Workload:
@@ -198,22 +199,22 @@ def tiny_nan(seed: int = 0) -> Workload:
     return w
 
 
-def llama3_8b(seed: int = 0, batch: int = 64) -> Workload:
+def llama3_8b(seed: int = 0, batch: int = 64, block_tokens: int = BLOCK_TOKENS) -> Workload:
     r = _rng(seed, _TAG_PARAMS, 0)
     ctx = _lognormal_lengths(r, batch, 1024, 1.0, 1, 8192)
     return _decode_batch(
         "llama3_8b_b64", "Llama-3-8B geometry, batch 64, lognormal(1024, 1.0) ctx in [1, 8192]",
-        seed, 32, 8, ctx)
+        seed, 32, 8, ctx, block_tokens=block_tokens)
 
 
-def llama33_70b(seed: int = 0, batch: int = 256) -> Workload:
+def llama33_70b(seed: int = 0, batch: int = 256, block_tokens: int = BLOCK_TOKENS) -> Workload:
     r = _rng(seed, _TAG_PARAMS, 0)
     ctx = _lognormal_lengths(r, batch, 4096, 1.2, 16, 131072)
     ctx[:4] = 131072
     return _decode_batch(
         "llama33_70b_b256",
         "Llama-3.3-70B geometry, batch 256, lognormal(4096, 1.2) ctx in [16, 131072], seqs 0-3 at 131072",
-        seed, 64, 8, ctx)
+        seed, 64, 8, ctx, block_tokens=block_tokens)
 
 
 def prefix_admission(seed: int = 0) -> Workload:
