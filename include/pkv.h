@@ -282,6 +282,31 @@ pkv_status pkv_attn_decode_static(const void* q, const void* k_cache, const void
  *    copy-on-write paragraph);
  *  - free pages are handed out in free_order (ascending ids if NULL); a
  *    released page is the next one handed out.
+ *
+ * Options of pkv_bm_create_ex (all off in pkv_bm_create):
+ *  - incremental: admission reserves only the prompt's pages,
+ *    ceil(prompt_len / block_tokens), and leaves at least watermark_blocks
+ *    pages available; a token that starts a new block, or a write into a
+ *    shared block, takes a page when pkv_bm_prepare_append reaches it, and a
+ *    step whose pages are not all available fails with PKV_ENOMEM and no
+ *    state change. The caller then preempts a sequence (pkv_bm_preempt, the
+ *    newest running one by pkv_bm_newest_running) and retries; the
+ *    preempted sequence keeps its token count and is later re-admitted by
+ *    pkv_bm_resume onto fresh pages for its KV to be recomputed (cs2680
+ *    Lecture 10, §10.5: on-demand pages run out, a watermark keeps
+ *    preemption rare, a preempted sequence is recomputed; "Reserve the page
+ *    a request has not written yet", "Pick a reservation policy you can
+ *    explain"). Fork under this policy reserves nothing.
+ *  - prefix_cache: pkv_bm_admit_tokens indexes every complete prompt block
+ *    by its exact token prefix and reuses indexed blocks for a later prompt
+ *    from its first block up to its first mismatch (a block is reusable iff
+ *    all its tokens and all earlier blocks match: 8,000 matching tokens
+ *    reuse 500 blocks of 16). A released indexed block stays cached instead
+ *    of returning to the free list; a cached block in use is never evicted,
+ *    and allocation, once the free list is empty, evicts the least recently
+ *    released idle cached block that no cached block extends ("KV cache
+ *    systems", prefix-hit and eviction paragraphs). Idle cached blocks count
+ *    as available to every admission and step.
  * A call that returns an error changes no state.
  * ------------------------------------------------------------------------- */
 typedef struct pkv_bm pkv_bm;
@@ -295,12 +320,23 @@ typedef struct pkv_bm_stats_t {
     int32_t num_seqs;
     int64_t ref_sum;       /* sum of refcounts == sum of table lengths */
     int64_t cow_copies;    /* copy-on-write pairs reported so far */
+    int32_t cached_blocks;      /* in the prefix index */
+    int32_t cached_idle_blocks; /* in the prefix index with refcount 0 */
+    int32_t preempted_seqs;
+    int32_t available_blocks;   /* free_blocks + cached_idle_blocks */
+    int64_t cache_hits;         /* blocks reused by pkv_bm_admit_tokens so far */
+    int64_t evictions;          /* cached blocks evicted so far */
 } pkv_bm_stats_t;
 
 /* free_order: host int32 permutation of [0, num_blocks), or NULL. Returns NULL
  * on invalid arguments. block_tokens: 8, 16, 32 or 64 (16 is the size the
  * pages use and the one the other calls assume). */
 pkv_bm* pkv_bm_create(int num_blocks, int block_tokens, const int32_t* free_order);
+/* As pkv_bm_create, with the policy options above (incremental and
+ * prefix_cache: 0 or non-zero; watermark_blocks >= 0, used by admission and
+ * resume only). */
+pkv_bm* pkv_bm_create_ex(int num_blocks, int block_tokens, const int32_t* free_order,
+                         int incremental, int watermark_blocks, int prefix_cache);
 void pkv_bm_destroy(pkv_bm* bm);
 
 /* group < 0: no sharing (prefix_len ignored). group >= 0: 0 <= prefix_len <=
@@ -310,7 +346,15 @@ void pkv_bm_destroy(pkv_bm* bm);
 pkv_status pkv_bm_admit(pkv_bm* bm, int prompt_len, int max_new, int group,
                         int prefix_len, int* seq_id);
 
-/* child_ids: host int32 [n]. All-or-nothing. */
+/* Admission with the prompt's token ids (host int32 [prompt_len], read
+ * during the call only) on a manager created with prefix_cache: the
+ * sequence's leading complete blocks that are cached are shared, not
+ * charged, and *reused_blocks (may be NULL) receives their number; its other
+ * complete prompt blocks are indexed. PKV_EINVAL without prefix_cache. */
+pkv_status pkv_bm_admit_tokens(pkv_bm* bm, const int32_t* tokens, int prompt_len, int max_new,
+                               int* seq_id, int* reused_blocks);
+
+/* child_ids: host int32 [n]. All-or-nothing. The parent must be running. */
 pkv_status pkv_bm_fork(pkv_bm* bm, int parent_seq, int n, int32_t* child_ids);
 
 /* For each listed sequence (distinct ids, processed in order): the slot of
@@ -319,12 +363,29 @@ pkv_status pkv_bm_fork(pkv_bm* bm, int parent_seq, int n, int32_t* child_ids);
  *   slot_mapping_out : host int64 [n]
  *   cow_pairs_out    : host int32 [n][2] (at most one pair per sequence)
  *   n_pairs_out      : number of pairs written
- * PKV_ENOSPC if a sequence has no reserved slot left (nothing changes). */
+ * Sequences must be running. Full reservation: PKV_ENOSPC if a sequence has
+ * no reserved slot left. Incremental: PKV_ENOMEM if the step needs more pages
+ * than are available. Either way nothing changes. */
 pkv_status pkv_bm_prepare_append(pkv_bm* bm, const int32_t* seq_ids, int n,
                                  int64_t* slot_mapping_out, int32_t* cow_pairs_out,
                                  int* n_pairs_out);
 
+/* Ends a sequence (running or preempted) and releases its references. */
 pkv_status pkv_bm_free(pkv_bm* bm, int seq_id);
+
+/* Preemption by recompute: releases a running sequence's references (its
+ * table becomes empty) and keeps its context length; *released_blocks (may
+ * be NULL) receives its former table length. */
+pkv_status pkv_bm_preempt(pkv_bm* bm, int seq_id, int* released_blocks);
+
+/* Re-admits a preempted sequence on fresh private pages (its context length
+ * rounded up under incremental, its full allowance otherwise), leaving the
+ * watermark available; the caller recomputes the KV of its context_len
+ * tokens into them. PKV_ENOMEM leaves it preempted. */
+pkv_status pkv_bm_resume(pkv_bm* bm, int seq_id);
+
+/* Id of the most recently admitted running sequence, -1 if none. */
+int pkv_bm_newest_running(pkv_bm* bm);
 
 /* Block table of one sequence into out[0 .. capacity); *length = its length.
  * PKV_ERANGE if capacity is too small. */
@@ -335,7 +396,8 @@ pkv_status pkv_bm_context_len(pkv_bm* bm, int seq_id, int* context_len);
 
 /* Padded batch view: tables_out int32 [n][width] (unused entries -1) and
  * context_lens_out int32 [n], ready to copy to the device for
- * pkv_attn_decode. PKV_ERANGE if a table is longer than width. */
+ * pkv_attn_decode. PKV_ERANGE if a table is longer than width; PKV_EINVAL if
+ * a sequence is unknown or preempted. */
 pkv_status pkv_bm_batch_tables(pkv_bm* bm, const int32_t* seq_ids, int n,
                                int32_t* tables_out, int width, int32_t* context_lens_out);
 

@@ -39,7 +39,8 @@ EXPORTED = [
     "pkv_bm_admit", "pkv_bm_fork", "pkv_bm_prepare_append", "pkv_bm_free",
     "pkv_bm_block_table", "pkv_bm_context_len", "pkv_bm_batch_tables", "pkv_bm_stats",
     "pkv_bm_refcount", "pkv_attn_decode_static", "pkv_decode_step", "pkv_attn_decode_ex", "pkv_append_ex",
-    "pkv_block_copy_ex",
+    "pkv_block_copy_ex", "pkv_bm_create_ex", "pkv_bm_admit_tokens", "pkv_bm_preempt", "pkv_bm_resume",
+    "pkv_bm_newest_running",
 ]
 BLOCK_SIZES = (8, 16, 32, 64)
 
@@ -67,6 +68,9 @@ class StatsT(ctypes.Structure):
         ("used_blocks", ctypes.c_int32), ("shared_blocks", ctypes.c_int32),
         ("spare_blocks", ctypes.c_int32), ("num_seqs", ctypes.c_int32),
         ("ref_sum", ctypes.c_int64), ("cow_copies", ctypes.c_int64),
+        ("cached_blocks", ctypes.c_int32), ("cached_idle_blocks", ctypes.c_int32),
+        ("preempted_seqs", ctypes.c_int32), ("available_blocks", ctypes.c_int32),
+        ("cache_hits", ctypes.c_int64), ("evictions", ctypes.c_int64),
     ]
 
 
@@ -106,6 +110,11 @@ def _load() -> ctypes.CDLL:
         "pkv_bm_batch_tables": (i32, [vp, vp, i32, vp, i32, vp]),
         "pkv_bm_stats": (i32, [vp, vp]),
         "pkv_bm_refcount": (i32, [vp, i32]),
+        "pkv_bm_create_ex": (vp, [i32, i32, vp, i32, i32, i32]),
+        "pkv_bm_admit_tokens": (i32, [vp, vp, i32, i32, vp, vp]),
+        "pkv_bm_preempt": (i32, [vp, i32, vp]),
+        "pkv_bm_resume": (i32, [vp, i32]),
+        "pkv_bm_newest_running": (i32, [vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -326,19 +335,23 @@ def attn_decode_static(q, k_cache, v_cache, block_tables, context_lens, scale, o
 
 
 class BlockManager:
-    """Free list, refcounts, copy-on-write and page-rounded admission (C++)."""
+    """Free list, refcounts, copy-on-write, page-rounded admission, incremental
+    allocation with preemption, and the prefix-cache index (C++)."""
 
-    def __init__(self, num_blocks: int, block_tokens: int = BLOCK_TOKENS, free_order=None):
+    def __init__(self, num_blocks: int, block_tokens: int = BLOCK_TOKENS, free_order=None,
+                 incremental: bool = False, watermark: int = 0, prefix_cache: bool = False):
         order = None
         self._order_buf = None
         if free_order is not None:
             arr = (ctypes.c_int32 * num_blocks)(*[int(x) for x in free_order])
             self._order_buf = arr
             order = ctypes.cast(arr, ctypes.c_void_p)
-        self._h = _lib.pkv_bm_create(num_blocks, block_tokens, order)
+        self._h = _lib.pkv_bm_create_ex(num_blocks, block_tokens, order, int(incremental), watermark,
+                                        int(prefix_cache))
         if not self._h:
-            raise PkvError(PKV_EINVAL, "pkv_bm_create")
+            raise PkvError(PKV_EINVAL, "pkv_bm_create_ex")
         self.num_blocks = num_blocks
+        self.reused: dict[int, int] = {}
 
     def __del__(self):
         h = getattr(self, "_h", None)
@@ -346,10 +359,22 @@ class BlockManager:
             _lib.pkv_bm_destroy(h)
             self._h = None
 
-    def admit(self, prompt_len: int, max_new: int, group: int = -1, prefix_len: int = 0) -> int:
+    def admit(self, prompt_len: int, max_new: int, group: int = -1, prefix_len: int = 0, tokens=None) -> int:
+        """tokens (the prompt's ids) selects pkv_bm_admit_tokens; the number of
+        reused cached blocks is then kept in self.reused[seq_id]."""
         sid = ctypes.c_int(0)
-        _check(_lib.pkv_bm_admit(self._h, prompt_len, max_new, group, prefix_len, ctypes.byref(sid)),
-               "pkv_bm_admit")
+        if tokens is None:
+            _check(_lib.pkv_bm_admit(self._h, prompt_len, max_new, group, prefix_len, ctypes.byref(sid)),
+                   "pkv_bm_admit")
+            self.reused[sid.value] = 0
+            return sid.value
+        if group >= 0 or len(tokens) != prompt_len:
+            raise PkvError(PKV_EINVAL, "pkv_bm_admit_tokens: no group, one token per prompt position")
+        buf = (ctypes.c_int32 * max(prompt_len, 1))(*[int(t) for t in tokens])
+        reused = ctypes.c_int(0)
+        _check(_lib.pkv_bm_admit_tokens(self._h, buf, prompt_len, max_new, ctypes.byref(sid),
+                                        ctypes.byref(reused)), "pkv_bm_admit_tokens")
+        self.reused[sid.value] = reused.value
         return sid.value
 
     def fork(self, parent: int, n: int) -> list[int]:
@@ -370,6 +395,18 @@ class BlockManager:
 
     def free(self, seq_id: int) -> None:
         _check(_lib.pkv_bm_free(self._h, seq_id), "pkv_bm_free")
+        self.reused.pop(seq_id, None)
+
+    def preempt(self, seq_id: int) -> int:
+        n = ctypes.c_int(0)
+        _check(_lib.pkv_bm_preempt(self._h, seq_id, ctypes.byref(n)), "pkv_bm_preempt")
+        return n.value
+
+    def resume(self, seq_id: int) -> None:
+        _check(_lib.pkv_bm_resume(self._h, seq_id), "pkv_bm_resume")
+
+    def newest_running(self) -> int:
+        return int(_lib.pkv_bm_newest_running(self._h))
 
     def table(self, seq_id: int) -> list[int]:
         length = ctypes.c_int(0)
@@ -401,7 +438,9 @@ class BlockManager:
         _check(_lib.pkv_bm_stats(self._h, ctypes.byref(s)), "pkv_bm_stats")
         return {"free": s.free_blocks, "used": s.used_blocks, "shared": s.shared_blocks,
                 "ref_sum": s.ref_sum, "spares": s.spare_blocks, "cow_copies": s.cow_copies,
-                "seqs": s.num_seqs}
+                "seqs": s.num_seqs, "cached": s.cached_blocks, "cached_idle": s.cached_idle_blocks,
+                "available": s.available_blocks, "cache_hits": s.cache_hits, "evictions": s.evictions,
+                "preempted": s.preempted_seqs}
 
     def refcount(self, block: int) -> int:
         return int(_lib.pkv_bm_refcount(self._h, block))

@@ -155,3 +155,117 @@ def test_concurrent_admissions_never_overcommit(nat):
     for t in threads:
         t.join()
     assert len(admitted) == 1 and bm.stats()["used"] == 145
+
+
+def _same_policy_state(o, n):
+    assert o.stats() == n.stats()
+    for s in sorted(o.seqs):
+        assert o.table(s) == n.table(s)
+        assert o.context_len(s) == n.context_len(s)
+    for b in range(o.num_blocks):
+        assert o.ref[b] == n.refcount(b)
+    assert o.newest_running() == n.newest_running()
+
+
+@pytest.mark.parametrize("seed", range(10))
+@pytest.mark.parametrize("incremental,watermark,prefix_cache",
+                         [(True, 0, False), (True, 3, False), (False, 0, True), (True, 2, True)])
+def test_random_policies_match_oracle(nat, seed, incremental, watermark, prefix_cache):
+    """Incremental growth, watermark, preemption, resume and prefix-cache hits
+    and evictions decided identically (block ids included) by both managers."""
+    rnd = random.Random(1000 + seed)
+    bt = rnd.choice([8, 16])
+    nb = rnd.randint(6, 40)
+    order = rnd.sample(range(nb), nb) if seed % 2 else None
+    kw = dict(incremental=incremental, watermark=watermark, prefix_cache=prefix_cache)
+    o = obm.BlockManager(nb, bt, order, **kw)
+    n = nat.BlockManager(nb, bt, order, **kw)
+    prompts = []
+    for _ in range(300):
+        running = [s for s, q in o.seqs.items() if q.running]
+        stopped = [s for s, q in o.seqs.items() if not q.running]
+        op = rnd.random()
+        if op < 0.25 or not o.seqs:
+            plen = rnd.randint(0, 4 * bt)
+            if prefix_cache and plen and rnd.random() < 0.7:
+                if prompts and rnd.random() < 0.6:
+                    src = rnd.choice(prompts)
+                    keep = len(src) if rnd.random() < 0.5 else rnd.randint(0, len(src))
+                    p = (src[:keep] + [rnd.randrange(2) for _ in range(plen)])[:plen]
+                else:
+                    p = [rnd.randrange(2) for _ in range(plen)]
+                prompts.append(p)
+                args = (plen, rnd.randint(0, 2 * bt))
+                sid = _both(nat, lambda: o.admit(*args, tokens=p), lambda: n.admit(*args, tokens=p))
+                if sid is not None:
+                    assert o.reused[sid] == n.reused[sid]
+            else:
+                grp = rnd.choice([-1, -1, 0])
+                args = (plen, rnd.randint(1, 2 * bt), grp, bt * rnd.randint(0, plen // bt) if grp >= 0 else 0)
+                _both(nat, lambda: o.admit(*args), lambda: n.admit(*args))
+        elif op < 0.35 and running:
+            par, k = rnd.choice(running), rnd.randint(0, 2)
+            _both(nat, lambda: o.fork(par, k), lambda: n.fork(par, k))
+        elif op < 0.75 and running:
+            ids = rnd.sample(running, rnd.randint(1, len(running)))
+            r = _both(nat, lambda: o.prepare_append(ids), lambda: n.prepare_append(ids))
+            if r is None and incremental:  # refused: preempt the newest and go on
+                v = o.newest_running()
+                assert _both(nat, lambda: o.preempt(v), lambda: n.preempt(v)) is not None
+        elif op < 0.85 and stopped:
+            s = rnd.choice(stopped)
+            _both(nat, lambda: o.resume(s), lambda: n.resume(s))
+        elif op < 0.9 and running:
+            s = rnd.choice(running)
+            _both(nat, lambda: o.preempt(s), lambda: n.preempt(s))
+        elif op < 0.97 and o.seqs:
+            s = rnd.choice(sorted(o.seqs))
+            _both(nat, lambda: o.free(s), lambda: n.free(s))
+        else:  # invalid calls
+            if stopped:
+                s = stopped[0]
+                _both(nat, lambda: o.prepare_append([s]), lambda: n.prepare_append([s]))
+                _both(nat, lambda: o.fork(s, 1), lambda: n.fork(s, 1))
+                _both(nat, lambda: o.preempt(s), lambda: n.preempt(s))
+            if running:
+                s = running[0]
+                _both(nat, lambda: o.resume(s), lambda: n.resume(s))
+        _same_policy_state(o, n)
+
+
+def test_prefix_hit_worked_example_native(nat, golden):
+    g = golden["prefix_hit_8000"]
+    rnd = random.Random(0)
+    cached = [rnd.randrange(32000) for _ in range(g["matching_tokens"] + 200)]
+    bm = nat.BlockManager(2048, g["block_tokens"], prefix_cache=True)
+    first = bm.admit(len(cached), 1, tokens=cached)
+    req = list(cached)
+    req[g["matching_tokens"]] += 1
+    sid = bm.admit(len(req), 1, tokens=req)
+    assert bm.reused[sid] == g["reused_blocks"]
+    assert bm.table(sid)[: g["reused_blocks"]] == bm.table(first)[: g["reused_blocks"]]
+    with pytest.raises(nat.PkvError):  # tokens need a prefix-cache manager
+        nat.BlockManager(64).admit(4, 1, tokens=[1, 2, 3, 4])
+
+
+def test_incremental_admission_and_preemption_native(nat, golden):
+    g = golden["admission_32L"]
+    bm = nat.BlockManager(g["pool_pages"], incremental=True)
+    s0 = bm.admit(g["prompt_tokens"], g["output_tokens"])
+    s1 = bm.admit(g["prompt_tokens"], g["output_tokens"])
+    with pytest.raises(nat.PoolExhausted):
+        bm.admit(g["prompt_tokens"], g["output_tokens"])
+    with pytest.raises(nat.PoolExhausted):
+        bm.prepare_append([s0, s1])
+    assert bm.newest_running() == s1 and bm.preempt(s1) == g["prompt_only_pages"]
+    bm.prepare_append([s0])
+    assert bm.stats()["preempted"] == 1 and bm.context_len(s1) == g["prompt_tokens"]
+    with pytest.raises(nat.PoolExhausted):
+        bm.resume(s1)
+    bm.free(s0)
+    bm.resume(s1)
+    assert len(bm.table(s1)) == g["prompt_only_pages"]
+    held = nat.BlockManager(g["pool_pages"], incremental=True, watermark=16)
+    held.admit(g["prompt_tokens"], g["output_tokens"])
+    with pytest.raises(nat.PoolExhausted):
+        held.admit(g["prompt_tokens"], g["output_tokens"])

@@ -81,7 +81,7 @@ def _fails(pins):
     for pin in pins:
         try:
             pin()
-        except Exception:  # noqa: BLE001 - any failure counts as caught
+        except (Exception, pytest.fail.Exception):  # noqa: BLE001 - any failure counts as caught
             failures += 1
     return failures
 
@@ -128,3 +128,88 @@ def test_copy_without_refcount_is_caught(monkeypatch):
 
     monkeypatch.setattr(bmod.BlockManager, "prepare_append", prepare_append)
     assert _fails([tb.test_copy_on_write_refcount_board]) == 1
+
+
+# -- incremental policy and prefix cache -----------------------------------
+
+from tests import test_oracle_block_policies as tp  # noqa: E402
+
+
+def _policy_pins():
+    pins = [lambda: tp.test_prefix_hit_worked_example(GOLDEN), lambda: tp.test_two_users_share_system_prompt(GOLDEN),
+            tp.test_hits_are_prefix_only, tp.test_partial_prompt_block_is_not_indexed,
+            tp.test_eviction_is_lru_leaf_first_and_spares_pinned_blocks,
+            tp.test_eviction_prefers_least_recently_released, tp.test_hit_on_idle_block_is_not_double_counted,
+            lambda: tp.test_incremental_admits_more_than_full_reservation(GOLDEN),
+            lambda: tp.test_growth_failure_then_preempt_newest_then_resume(GOLDEN),
+            tp.test_watermark_binds_admission_and_resume_not_growth, tp.test_incremental_fork_copies_on_demand,
+            tp.test_preempted_prefix_blocks_stay_cached]
+    pins += [lambda s=s: tp.test_hits_match_brute_force(s) for s in range(3)]
+    return pins
+
+
+def test_block_local_cache_key_is_caught(monkeypatch):
+    # planted: a block keyed by its own tokens only, not by the prefix it ends
+    monkeypatch.setattr(bmod.BlockManager, "_block_key", lambda self, t, i: tuple(t[self.b * i: self.b * (i + 1)]))
+    assert _fails(_policy_pins()) >= 1
+
+
+def test_plain_lru_eviction_is_caught(monkeypatch):
+    def victim(self):  # planted: evicts an idle block that cached blocks still extend
+        idle = [blk for blk in self.key if self.ref[blk] == 0]
+        return min(idle, key=lambda blk: (self.last_use[blk], blk))
+
+    monkeypatch.setattr(bmod.BlockManager, "_victim", victim)
+    assert _fails(_policy_pins()) >= 1
+
+
+def test_most_recent_eviction_is_caught(monkeypatch):
+    def victim(self):  # planted: most recently released leaf
+        leaves = [blk for blk in self.key if self.ref[blk] == 0 and self.children.get(blk, 0) == 0]
+        return max(leaves, key=lambda blk: (self.last_use[blk], blk))
+
+    monkeypatch.setattr(bmod.BlockManager, "_victim", victim)
+    assert _fails(_policy_pins()) >= 1
+
+
+def test_counting_reused_idle_blocks_as_room_is_caught(monkeypatch):
+    monkeypatch.setattr(bmod.BlockManager, "_room", lambda self, hits: self.available())
+    assert _fails(_policy_pins()) >= 1
+
+
+def test_ignored_watermark_is_caught(monkeypatch):
+    real = bmod.BlockManager.__init__
+
+    def init(self, *a, **kw):
+        real(self, *a, **kw)
+        self.watermark = 0  # planted
+
+    monkeypatch.setattr(bmod.BlockManager, "__init__", init)
+    assert _fails(_policy_pins()) >= 1
+
+
+def test_incremental_reserving_the_output_is_caught(monkeypatch):
+    real = bmod.BlockManager.admit
+
+    def admit(self, prompt_len, max_new, group=-1, prefix_len=0, tokens=None):
+        inc = self.incremental
+        self.incremental = False  # planted: admission charges the output too
+        try:
+            return real(self, prompt_len, max_new, group, prefix_len, tokens)
+        finally:
+            self.incremental = inc
+
+    monkeypatch.setattr(bmod.BlockManager, "admit", admit)
+    assert _fails(_policy_pins()) >= 1
+
+
+def test_preemption_that_drops_tokens_is_caught(monkeypatch):
+    real = bmod.BlockManager.preempt
+
+    def preempt(self, sid):
+        n = real(self, sid)
+        self.seqs[sid].ctx = 0  # planted: the sequence restarts from nothing
+        return n
+
+    monkeypatch.setattr(bmod.BlockManager, "preempt", preempt)
+    assert _fails(_policy_pins()) >= 1
