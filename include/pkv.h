@@ -384,6 +384,14 @@ pkv_status pkv_bm_preempt(pkv_bm* bm, int seq_id, int* released_blocks);
  * tokens into them. PKV_ENOMEM leaves it preempted. */
 pkv_status pkv_bm_resume(pkv_bm* bm, int seq_id);
 
+/* Slots (block id * block_tokens + offset) of a running sequence's token
+ * positions [first, first + n) into slots_out (host int64 [n]): where a
+ * prefill, or the recompute after pkv_bm_resume, writes their KV with
+ * pkv_append. Positions must lie within the sequence's table (PKV_EINVAL
+ * otherwise). A position in a block shared with other sequences is shared
+ * too: writing it changes their KV. */
+pkv_status pkv_bm_slots(pkv_bm* bm, int seq_id, int first, int n, int64_t* slots_out);
+
 /* Id of the most recently admitted running sequence, -1 if none. */
 int pkv_bm_newest_running(pkv_bm* bm);
 

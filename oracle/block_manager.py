@@ -368,6 +368,14 @@ class BlockManager:
             self.ref[blk] = 1
         s.running = True
 
+    def slots(self, sid: int, first: int, n: int) -> list[int]:
+        """Slots of a running sequence's token positions [first, first + n),
+        within its table: where a prefill or a recompute writes their KV."""
+        s = self.seqs.get(sid)
+        if s is None or not s.running or first < 0 or n < 0 or first + n > len(s.table) * self.b:
+            raise InvalidRequest("unknown or preempted sequence, or positions outside its table")
+        return [s.table[p // self.b] * self.b + p % self.b for p in range(first, first + n)]
+
     def newest_running(self) -> int:
         running = [sid for sid, s in self.seqs.items() if s.running]
         return max(running) if running else -1

@@ -40,7 +40,7 @@ EXPORTED = [
     "pkv_bm_block_table", "pkv_bm_context_len", "pkv_bm_batch_tables", "pkv_bm_stats",
     "pkv_bm_refcount", "pkv_attn_decode_static", "pkv_decode_step", "pkv_attn_decode_ex", "pkv_append_ex",
     "pkv_block_copy_ex", "pkv_bm_create_ex", "pkv_bm_admit_tokens", "pkv_bm_preempt", "pkv_bm_resume",
-    "pkv_bm_newest_running",
+    "pkv_bm_newest_running", "pkv_bm_slots",
 ]
 BLOCK_SIZES = (8, 16, 32, 64)
 
@@ -115,6 +115,7 @@ def _load() -> ctypes.CDLL:
         "pkv_bm_preempt": (i32, [vp, i32, vp]),
         "pkv_bm_resume": (i32, [vp, i32]),
         "pkv_bm_newest_running": (i32, [vp]),
+        "pkv_bm_slots": (i32, [vp, i32, i32, i32, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -407,6 +408,11 @@ class BlockManager:
 
     def newest_running(self) -> int:
         return int(_lib.pkv_bm_newest_running(self._h))
+
+    def slots(self, seq_id: int, first: int, n: int) -> list[int]:
+        buf = (ctypes.c_int64 * max(n, 1))()
+        _check(_lib.pkv_bm_slots(self._h, seq_id, first, n, buf), "pkv_bm_slots")
+        return list(buf[:n])
 
     def table(self, seq_id: int) -> list[int]:
         length = ctypes.c_int(0)

@@ -449,6 +449,20 @@ pkv_status pkv_bm_resume(pkv_bm* bm, int seq_id) {
     return PKV_OK;
 }
 
+pkv_status pkv_bm_slots(pkv_bm* bm, int seq_id, int first, int n, int64_t* slots_out) {
+    if (!bm || first < 0 || n < 0 || (n > 0 && !slots_out)) return PKV_EINVAL;
+    std::lock_guard<std::mutex> lock(bm->mu);
+    const Sequence* s = bm->running_seq(seq_id);
+    const int64_t bt = bm->block_tokens;
+    if (!s || static_cast<int64_t>(first) + n > static_cast<int64_t>(s->table.size()) * bt)
+        return PKV_EINVAL;
+    for (int i = 0; i < n; ++i) {
+        const int64_t pos = static_cast<int64_t>(first) + i;
+        slots_out[i] = static_cast<int64_t>(s->table[pos / bt]) * bt + pos % bt;
+    }
+    return PKV_OK;
+}
+
 int pkv_bm_newest_running(pkv_bm* bm) {
     if (!bm) return -1;
     std::lock_guard<std::mutex> lock(bm->mu);

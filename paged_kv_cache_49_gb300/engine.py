@@ -48,7 +48,8 @@ class StepBuffers:
 
 class PagedKVEngine:
     def __init__(self, num_blocks: int, num_q_heads: int, num_kv_heads: int, head_dim: int = 128,
-                 device="cuda", free_order=None, block_tokens: int = nat.BLOCK_TOKENS):
+                 device="cuda", free_order=None, block_tokens: int = nat.BLOCK_TOKENS, incremental: bool = False,
+                 watermark: int = 0, prefix_cache: bool = False):
         self.num_blocks, self.num_q_heads, self.num_kv_heads, self.head_dim = (
             num_blocks, num_q_heads, num_kv_heads, head_dim)
         self.block_tokens = block_tokens
@@ -56,7 +57,8 @@ class PagedKVEngine:
         shape = (num_blocks, num_kv_heads, block_tokens, head_dim)
         self.k_cache = torch.empty(shape, dtype=torch.bfloat16, device=self.device)
         self.v_cache = torch.empty(shape, dtype=torch.bfloat16, device=self.device)
-        self.bm = nat.BlockManager(num_blocks, block_tokens, free_order)
+        self.bm = nat.BlockManager(num_blocks, block_tokens, free_order, incremental=incremental,
+                                   watermark=watermark, prefix_cache=prefix_cache)
         self.error = nat.new_error_word(self.device)
 
     # ---- pool content ----------------------------------------------------
@@ -81,6 +83,15 @@ class PagedKVEngine:
         st = torch.tensor(slots, dtype=torch.int64).to(self.device, non_blocking=True)
         nat.append(k, v, st, self.k_cache, self.v_cache, self.error, stream)
         return slots, pairs
+
+    def write_positions(self, seq_id: int, first: int, k: torch.Tensor, v: torch.Tensor, stream=None):
+        """Write the KV of token positions [first, first + n) of one sequence
+        (k, v: [n, Hkv, D] bf16 on device) -- a prefill, or the recompute of a
+        resumed sequence -- with the append kernel; returns the slots."""
+        slots = self.bm.slots(seq_id, first, int(k.shape[0]))
+        st = torch.tensor(slots, dtype=torch.int64).to(self.device, non_blocking=True)
+        nat.append(k, v, st, self.k_cache, self.v_cache, self.error, stream)
+        return slots
 
     def replay_events(self, w, with_content: bool = True):
         """Apply a workload's admit / fork / history events; history appends

@@ -157,7 +157,7 @@ def test_concurrent_admissions_never_overcommit(nat):
     assert len(admitted) == 1 and bm.stats()["used"] == 145
 
 
-def _same_policy_state(o, n):
+def _same_policy_state(nat, o, n):
     assert o.stats() == n.stats()
     for s in sorted(o.seqs):
         assert o.table(s) == n.table(s)
@@ -165,6 +165,11 @@ def _same_policy_state(o, n):
     for b in range(o.num_blocks):
         assert o.ref[b] == n.refcount(b)
     assert o.newest_running() == n.newest_running()
+    for s in sorted(o.seqs):
+        if o.seqs[s].running:
+            cap = len(o.table(s)) * o.b
+            assert o.slots(s, 0, cap) == n.slots(s, 0, cap)
+            _both(nat, lambda: o.slots(s, 1, cap), lambda: n.slots(s, 1, cap))  # one past the table
 
 
 @pytest.mark.parametrize("seed", range(10))
@@ -230,7 +235,7 @@ def test_random_policies_match_oracle(nat, seed, incremental, watermark, prefix_
             if running:
                 s = running[0]
                 _both(nat, lambda: o.resume(s), lambda: n.resume(s))
-        _same_policy_state(o, n)
+        _same_policy_state(nat, o, n)
 
 
 def test_prefix_hit_worked_example_native(nat, golden):
