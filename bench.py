@@ -365,56 +365,44 @@ def run_ours(args):
     if eng.read_errors(sb):
         raise RuntimeError("device error word set during the timed steps")
 
-    # ---- end to end through the public API from pinned host buffers ----
+    # ---- end to end through the C ABI's host-buffer step ----
+    # Every step: one copy of the packed inputs from pinned host memory, the
+    # step's kernels, one copy of the output rows back (pkv_decode_step_host).
     e2e = None
     if not args.no_e2e:
-        host = {name: getattr(sb, name).cpu().pin_memory()
-                for name in ("q", "k", "v", "slots", "pairs", "tables", "ctx")}
-        out_host = torch.empty(sb.out.shape, dtype=sb.out.dtype).pin_memory()
-        h2d = sum(t.numel() * t.element_size() for t in host.values())
-        d2h = out_host.numel() * out_host.element_size()
-        ees = []
-        for i in range(args.warmup + args.steps):
-            flush(i)
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for name, t in host.items():
-                getattr(sb, name).copy_(t, non_blocking=True)
-            eng.run_step(sb, w.scale, args.num_ctas)
-            out_host.copy_(sb.out, non_blocking=True)
-            e1.record(stream)
-            e1.synchronize()
-            if i >= args.warmup:
-                ees.append(e0.elapsed_time(e1))
-        e2e_ms = statistics.mean(ees)
-        if world > 1:
-            t = torch.tensor([e2e_ms], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        hs = pkv.HostStep(eng, B, sb.tables.shape[1], max_pairs=max(1, sb.num_pairs))
+        h2d = hs.pack(sb.q.cpu(), sb.k.cpu(), sb.v.cpu(), sb.slots.cpu(), sb.tables.cpu(), sb.ctx.cpu(),
+                      sb.pairs.cpu() if sb.num_pairs else None)
+        d2h = hs.out_host.numel() * hs.out_host.element_size()
+
+        def timed(run):
+            ts = []
+            for i in range(args.warmup + args.steps):
+                flush(i)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                run()
+                e1.record(stream)
+                e1.synchronize()
+                if i >= args.warmup:
+                    ts.append(e0.elapsed_time(e1))
+            t_ms = statistics.mean(ts)
+            if world > 1:
+                t = torch.tensor([t_ms], device="cuda")
+                dist.all_reduce(t, op=dist.ReduceOp.MAX)
+                t_ms = float(t.item())
+            return t_ms
+
+        e2e_ms = timed(lambda: hs.run(w.scale, args.num_ctas))
+        if not torch.equal(hs.out_host, sb.out.cpu()):
+            raise RuntimeError("host-buffer step output differs from the device step")
         e2e = {"value": B * world / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
-        # The same, with the step replayed from a CUDA graph (as a server does).
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "call": "pkv_decode_step_host"}
+        # The same call captured once in a CUDA graph and replayed (as a server does).
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
-            eng.run_step(sb, w.scale, args.num_ctas)
-        gts = []
-        for i in range(args.warmup + args.steps):
-            flush(i)
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for name, t in host.items():
-                getattr(sb, name).copy_(t, non_blocking=True)
-            graph.replay()
-            out_host.copy_(sb.out, non_blocking=True)
-            e1.record(stream)
-            e1.synchronize()
-            if i >= args.warmup:
-                gts.append(e0.elapsed_time(e1))
-        g_ms = statistics.mean(gts)
-        if world > 1:
-            t = torch.tensor([g_ms], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            g_ms = float(t.item())
+            hs.run(w.scale, args.num_ctas)
+        g_ms = timed(graph.replay)
         e2e["graph_replay"] = {"value": B * world / (g_ms * 1e-3), "ms_per_step": g_ms}
 
     if rank != 0:

@@ -220,6 +220,42 @@ pkv_status pkv_decode_step(const void* k_new, const void* v_new, const int64_t* 
                            int num_kv_heads, int head_dim, float scale, int num_ctas, void* workspace,
                            size_t workspace_bytes, void* out, uint32_t* device_error, void* stream);
 
+/*
+ * pkv_step_layout -- where the inputs of one decode step sit in one packed
+ * buffer for pkv_decode_step_host, in this order, each 256-byte aligned:
+ * q [num_seqs][Hq][D] bf16, k_new and v_new [num_seqs][Hkv][D] bf16,
+ * slot_mapping [num_seqs] int64, block_tables [num_seqs][max_blocks_per_seq]
+ * int32, context_lens [num_seqs] int32, src_dst_pairs [num_pairs][2] int32
+ * (last, so that no other offset depends on num_pairs); bytes = the
+ * buffer's size. One new token per sequence (slot -1 for a padding row).
+ */
+typedef struct pkv_step_layout_t {
+    size_t q, k_new, v_new, slot_mapping, block_tables, context_lens, src_dst_pairs;
+    size_t bytes;
+} pkv_step_layout_t;
+
+pkv_status pkv_step_layout(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                           int max_blocks_per_seq, int num_pairs, pkv_step_layout_t* layout);
+
+/*
+ * pkv_decode_step_host -- pkv_decode_step with its inputs and output in host
+ * memory: one copy of host_packed (laid out by pkv_step_layout; pinned
+ * memory makes the copy asynchronous and fast) into device_staging (device,
+ * layout.bytes, 256-byte aligned), the step itself reading its inputs from
+ * there and writing attention rows to device_out (device, [num_seqs][Hq][D]
+ * bf16), then one copy of those rows into host_out. Everything is enqueued
+ * on `stream` and checked before anything is enqueued: host_packed must not
+ * change, and host_out must not be read, until the stream has passed the
+ * step (e.g. after cudaStreamSynchronize). This is the call through which a
+ * host program that keeps its step inputs in host memory drives a step.
+ */
+pkv_status pkv_decode_step_host(const void* host_packed, void* device_staging, int num_pairs,
+                                void* k_cache, void* v_cache, int num_blocks, int max_blocks_per_seq,
+                                int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                float scale, int num_ctas, void* workspace, size_t workspace_bytes,
+                                void* device_out, void* host_out, uint32_t* device_error,
+                                void* stream);
+
 /* Number of persistent CTAs pkv_attn_decode launches for num_seqs sequences
  * when num_ctas == 0 (every CTA that fits on the current device at once);
  * 0 on error. */

@@ -40,7 +40,7 @@ EXPORTED = [
     "pkv_bm_block_table", "pkv_bm_context_len", "pkv_bm_batch_tables", "pkv_bm_stats",
     "pkv_bm_refcount", "pkv_attn_decode_static", "pkv_decode_step", "pkv_attn_decode_ex", "pkv_append_ex",
     "pkv_block_copy_ex", "pkv_bm_create_ex", "pkv_bm_admit_tokens", "pkv_bm_preempt", "pkv_bm_resume",
-    "pkv_bm_newest_running", "pkv_bm_slots",
+    "pkv_bm_newest_running", "pkv_bm_slots", "pkv_step_layout", "pkv_decode_step_host",
 ]
 BLOCK_SIZES = (8, 16, 32, 64)
 
@@ -72,6 +72,11 @@ class StatsT(ctypes.Structure):
         ("preempted_seqs", ctypes.c_int32), ("available_blocks", ctypes.c_int32),
         ("cache_hits", ctypes.c_int64), ("evictions", ctypes.c_int64),
     ]
+
+
+class StepLayoutT(ctypes.Structure):
+    _fields_ = [(name, ctypes.c_size_t) for name in
+                ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens", "src_dst_pairs", "bytes")]
 
 
 def _load() -> ctypes.CDLL:
@@ -116,6 +121,9 @@ def _load() -> ctypes.CDLL:
         "pkv_bm_resume": (i32, [vp, i32]),
         "pkv_bm_newest_running": (i32, [vp]),
         "pkv_bm_slots": (i32, [vp, i32, i32, i32, vp]),
+        "pkv_step_layout": (i32, [i32, i32, i32, i32, i32, i32, vp]),
+        "pkv_decode_step_host": (i32, [vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, i32, f32, i32, vp, sz, vp, vp,
+                                       vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -305,6 +313,43 @@ def decode_step(q, k_new, v_new, slot_mapping, pairs, k_cache, v_cache, block_ta
                                 int(num_ctas), workspace.ptr, workspace.nbytes, _ptr(out), _ptr(device_error),
                                 _stream(stream)), "pkv_decode_step")
     return out
+
+
+def step_layout(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int, max_blocks_per_seq: int,
+                num_pairs: int = 0) -> dict:
+    """Byte offsets (and total size) of a decode step's inputs in one packed buffer."""
+    lay = StepLayoutT()
+    _check(_lib.pkv_step_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, num_pairs,
+                                ctypes.byref(lay)), "pkv_step_layout")
+    return {name: int(getattr(lay, name)) for name, _ in StepLayoutT._fields_}
+
+
+def decode_step_host(host_packed, device_staging, num_pairs, k_cache, v_cache, max_blocks_per_seq, num_seqs,
+                     num_q_heads, scale, workspace, device_out, host_out, device_error=None, num_ctas: int = 0,
+                     stream=None) -> None:
+    """pkv_decode_step_host: one H2D copy of the packed inputs (pinned uint8
+    host tensor), the step, one D2H copy of the output rows into host_out."""
+    _need(host_packed, torch.uint8, "host_packed", cuda=False)
+    _need(device_staging, torch.uint8, "device_staging")
+    _need(k_cache, torch.bfloat16, "k_cache")
+    _need(v_cache, torch.bfloat16, "v_cache")
+    _need(device_out, torch.bfloat16, "device_out")
+    _need(host_out, torch.bfloat16, "host_out", cuda=False)
+    if host_packed.is_cuda or host_out.is_cuda:
+        raise ValueError("host_packed and host_out must be host tensors (pinned for asynchronous copies)")
+    nb, hkv, bt, d = k_cache.shape
+    if bt != BLOCK_TOKENS or v_cache.shape != k_cache.shape:
+        raise ValueError("caches must be [NB, Hkv, 16, D] and alike")
+    if device_out.shape != (num_seqs, num_q_heads, d) or host_out.shape != device_out.shape:
+        raise ValueError("device_out and host_out must be [num_seqs, Hq, D]")
+    need = step_layout(num_seqs, num_q_heads, hkv, d, max_blocks_per_seq, num_pairs)["bytes"]
+    if host_packed.numel() < need or device_staging.numel() < need:
+        raise ValueError(f"packed buffers need {need} bytes")
+    _check(_lib.pkv_decode_step_host(_ptr(host_packed), _ptr(device_staging), num_pairs, _ptr(k_cache),
+                                     _ptr(v_cache), nb, max_blocks_per_seq, num_seqs, num_q_heads, hkv, d,
+                                     float(scale), int(num_ctas), workspace.ptr, workspace.nbytes,
+                                     _ptr(device_out), _ptr(host_out), _ptr(device_error), _stream(stream)),
+           "pkv_decode_step_host")
 
 
 def attn_decode_static(q, k_cache, v_cache, block_tables, context_lens, scale, out, device_error=None,

@@ -943,6 +943,61 @@ pkv_status pkv_attn_decode_ex(const void* q, const void* k_cache, const void* v_
     return attn::launch(L, as_stream(stream), false);
 }
 
+}  // extern "C"
+
+namespace {
+
+// The checks of pkv_decode_step that come before anything is enqueued; on
+// success L holds the attention launch.
+pkv_status check_step(const void* k_new, const void* v_new, const int64_t* slot_mapping, int num_new_tokens,
+                      const int32_t* src_dst_pairs, int num_pairs, void* k_cache, void* v_cache, int num_blocks,
+                      const void* q, const int32_t* block_tables, int max_blocks_per_seq,
+                      const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads,
+                      int head_dim, float scale, int num_ctas, void* workspace, size_t workspace_bytes,
+                      void* out, attn::Launch* L) {
+    if (num_new_tokens < 0 || num_pairs < 0) return PKV_EINVAL;
+    const pkv_status st =
+        attn::prepare(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs, num_q_heads,
+                      num_kv_heads, head_dim, num_blocks, scale, num_ctas, workspace, workspace_bytes, out, L);
+    if (st != PKV_OK) return st;
+    if (num_pairs > 65535) return PKV_ERANGE;
+    if ((num_pairs > 0 && !src_dst_pairs) || (num_new_tokens > 0 && (!k_new || !v_new || !slot_mapping)))
+        return PKV_EINVAL;
+    if (num_new_tokens > 0 && (!aligned16(k_new) || !aligned16(v_new))) return PKV_EINVAL;
+    return PKV_OK;
+}
+
+// The launches of a checked step: block copy, append (warming L2 with the
+// attention's cold inputs while it runs), attention launched early.
+pkv_status enqueue_step(const attn::Launch& L, const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                        int num_new_tokens, const int32_t* src_dst_pairs, int num_pairs, void* k_cache,
+                        void* v_cache, int num_blocks, int num_kv_heads, int head_dim,
+                        uint32_t* device_error, void* stream) {
+    pkv_status st = PKV_OK;
+    if (num_pairs > 0) {
+        st = pkv_block_copy(k_cache, v_cache, src_dst_pairs, num_pairs, num_blocks, num_kv_heads, head_dim,
+                            device_error, stream);
+        if (st != PKV_OK) return st;
+    }
+    if (num_new_tokens > 0) {
+        const attn::Params& p = L.prm;
+        const L2Warm warm = {{p.block_tables, p.q, p.context_lens},
+                             {static_cast<size_t>(p.num_seqs) * p.max_blocks * 4,
+                              static_cast<size_t>(p.num_seqs) * p.num_q_heads * head_dim * 2,
+                              static_cast<size_t>(p.num_seqs) * 4}};
+        st = launch_append(k_new, v_new, slot_mapping, num_new_tokens, k_cache, v_cache, num_blocks, num_kv_heads,
+                           head_dim, PKV_BLOCK_TOKENS, device_error, stream, &warm);
+        if (st != PKV_OK) return st;
+    }
+    return attn::launch(L, as_stream(stream), num_pairs > 0 || num_new_tokens > 0);
+}
+
+size_t align_up256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+
+extern "C" {
+
 pkv_status pkv_decode_step(const void* k_new, const void* v_new, const int64_t* slot_mapping,
                            int num_new_tokens, const int32_t* src_dst_pairs, int num_pairs,
                            void* k_cache, void* v_cache, int num_blocks, const void* q,
@@ -950,33 +1005,80 @@ pkv_status pkv_decode_step(const void* k_new, const void* v_new, const int64_t* 
                            const int32_t* context_lens, int num_seqs, int num_q_heads,
                            int num_kv_heads, int head_dim, float scale, int num_ctas, void* workspace,
                            size_t workspace_bytes, void* out, uint32_t* device_error, void* stream) {
-    if (num_new_tokens < 0 || num_pairs < 0) return PKV_EINVAL;
-    // Validate the whole step before launching any part of it.
     attn::Launch L;
-    pkv_status st = attn::prepare(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
-                                  num_seqs, num_q_heads, num_kv_heads, head_dim, num_blocks, scale, num_ctas,
-                                  workspace, workspace_bytes, out, &L);
+    const pkv_status st = check_step(k_new, v_new, slot_mapping, num_new_tokens, src_dst_pairs, num_pairs, k_cache,
+                                     v_cache, num_blocks, q, block_tables, max_blocks_per_seq, context_lens,
+                                     num_seqs, num_q_heads, num_kv_heads, head_dim, scale, num_ctas, workspace,
+                                     workspace_bytes, out, &L);
     if (st != PKV_OK) return st;
-    if (num_pairs > 65535) return PKV_ERANGE;
-    if ((num_pairs > 0 && !src_dst_pairs) || (num_new_tokens > 0 && (!k_new || !v_new || !slot_mapping)))
+    return enqueue_step(L, k_new, v_new, slot_mapping, num_new_tokens, src_dst_pairs, num_pairs, k_cache, v_cache,
+                        num_blocks, num_kv_heads, head_dim, device_error, stream);
+}
+
+pkv_status pkv_step_layout(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int max_blocks_per_seq,
+                           int num_pairs, pkv_step_layout_t* layout) {
+    if (!layout || num_seqs < 1 || num_q_heads < 1 || num_kv_heads < 1 || head_dim < 1 || max_blocks_per_seq < 1 ||
+        num_pairs < 0)
         return PKV_EINVAL;
-    if (num_new_tokens > 0 && (!aligned16(k_new) || !aligned16(v_new))) return PKV_EINVAL;
-    if (num_pairs > 0) {
-        st = pkv_block_copy(k_cache, v_cache, src_dst_pairs, num_pairs, num_blocks, num_kv_heads, head_dim,
-                            device_error, stream);
-        if (st != PKV_OK) return st;
+    if (num_seqs > PKV_ATTN_MAX_SEQS || num_pairs > 65535) return PKV_ERANGE;
+    const size_t B = static_cast<size_t>(num_seqs);
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off = align_up256(off + bytes);
+        return at;
+    };
+    layout->q = take(B * num_q_heads * head_dim * 2);
+    layout->k_new = take(B * num_kv_heads * head_dim * 2);
+    layout->v_new = take(B * num_kv_heads * head_dim * 2);
+    layout->slot_mapping = take(B * 8);
+    layout->block_tables = take(B * max_blocks_per_seq * 4);
+    layout->context_lens = take(B * 4);
+    layout->src_dst_pairs = take(static_cast<size_t>(num_pairs) * 8);  // last: no other offset depends on it
+    layout->bytes = off;
+    return PKV_OK;
+}
+
+pkv_status pkv_decode_step_host(const void* host_packed, void* device_staging, int num_pairs, void* k_cache,
+                                void* v_cache, int num_blocks, int max_blocks_per_seq, int num_seqs,
+                                int num_q_heads, int num_kv_heads, int head_dim, float scale, int num_ctas,
+                                void* workspace, size_t workspace_bytes, void* device_out, void* host_out,
+                                uint32_t* device_error, void* stream) {
+    if (!host_packed || !device_staging || !host_out || !device_out) return PKV_EINVAL;
+    if (reinterpret_cast<uintptr_t>(device_staging) & 255u) return PKV_EINVAL;
+    pkv_step_layout_t lay;
+    pkv_status st = pkv_step_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, num_pairs,
+                                    &lay);
+    if (st != PKV_OK) return st;
+    uint8_t* d = static_cast<uint8_t*>(device_staging);
+    const void* q = d + lay.q;
+    const void* k_new = d + lay.k_new;
+    const void* v_new = d + lay.v_new;
+    const int64_t* slots = reinterpret_cast<const int64_t*>(d + lay.slot_mapping);
+    const int32_t* pairs = num_pairs > 0 ? reinterpret_cast<const int32_t*>(d + lay.src_dst_pairs) : nullptr;
+    const int32_t* tables = reinterpret_cast<const int32_t*>(d + lay.block_tables);
+    const int32_t* ctx = reinterpret_cast<const int32_t*>(d + lay.context_lens);
+    attn::Launch L;
+    st = check_step(k_new, v_new, slots, num_seqs, pairs, num_pairs, k_cache, v_cache, num_blocks, q, tables,
+                    max_blocks_per_seq, ctx, num_seqs, num_q_heads, num_kv_heads, head_dim, scale, num_ctas,
+                    workspace, workspace_bytes, device_out, &L);
+    if (st != PKV_OK) return st;
+    cudaStream_t s = as_stream(stream);
+    cudaError_t e = cudaMemcpyAsync(device_staging, host_packed, lay.bytes, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) {
+        record_cuda_error(e);
+        return PKV_ECUDA;
     }
-    if (num_new_tokens > 0) {
-        // While the append runs, warm L2 with the attention's cold inputs.
-        const L2Warm warm = {{block_tables, q, context_lens},
-                             {static_cast<size_t>(num_seqs) * max_blocks_per_seq * 4,
-                              static_cast<size_t>(num_seqs) * num_q_heads * head_dim * 2,
-                              static_cast<size_t>(num_seqs) * 4}};
-        st = launch_append(k_new, v_new, slot_mapping, num_new_tokens, k_cache, v_cache, num_blocks, num_kv_heads,
-                           head_dim, PKV_BLOCK_TOKENS, device_error, stream, &warm);
-        if (st != PKV_OK) return st;
+    st = enqueue_step(L, k_new, v_new, slots, num_seqs, pairs, num_pairs, k_cache, v_cache, num_blocks,
+                      num_kv_heads, head_dim, device_error, stream);
+    if (st != PKV_OK) return st;
+    e = cudaMemcpyAsync(host_out, device_out, static_cast<size_t>(num_seqs) * num_q_heads * head_dim * 2,
+                        cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) {
+        record_cuda_error(e);
+        return PKV_ECUDA;
     }
-    return attn::launch(L, as_stream(stream), num_pairs > 0 || num_new_tokens > 0);
+    return PKV_OK;
 }
 
 }  // extern "C"

@@ -161,3 +161,68 @@ class PagedKVEngine:
         if sb is not None:
             e |= sb.workspace.read_error()
         return e
+
+
+class HostStep:
+    """A decode step whose inputs and output live in host memory: one pinned
+    packed input buffer (laid out by pkv_step_layout), its device staging
+    copy, and pinned output rows. run() is one pkv_decode_step_host call:
+    one host-to-device copy, the step's kernels, one device-to-host copy."""
+
+    _DTYPES = {"q": torch.bfloat16, "k_new": torch.bfloat16, "v_new": torch.bfloat16, "slot_mapping": torch.int64,
+               "block_tables": torch.int32, "context_lens": torch.int32, "src_dst_pairs": torch.int32}
+
+    def __init__(self, eng: PagedKVEngine, num_seqs: int, width: int, max_pairs: int = 0):
+        if eng.block_tokens != nat.BLOCK_TOKENS:
+            raise ValueError("host-buffer steps use 16-token blocks")
+        self.eng, self.num_seqs, self.width, self.max_pairs = eng, num_seqs, width, max_pairs
+        hq, hkv, d = eng.num_q_heads, eng.num_kv_heads, eng.head_dim
+        self.layout = nat.step_layout(num_seqs, hq, hkv, d, width, max_pairs)
+        self.shapes = {"q": (num_seqs, hq, d), "k_new": (num_seqs, hkv, d), "v_new": (num_seqs, hkv, d),
+                       "slot_mapping": (num_seqs,), "block_tables": (num_seqs, width),
+                       "context_lens": (num_seqs,), "src_dst_pairs": (max_pairs, 2)}
+        nbytes = self.layout["bytes"]
+        self.host = torch.zeros(nbytes, dtype=torch.uint8).pin_memory()
+        buf = torch.empty(nbytes + 256, dtype=torch.uint8, device=eng.device)
+        off = (-buf.data_ptr()) % 256
+        self._staging_buf, self.staging = buf, buf[off: off + nbytes]
+        self.out_dev = torch.empty((num_seqs, hq, d), dtype=torch.bfloat16, device=eng.device)
+        self.out_host = torch.empty((num_seqs, hq, d), dtype=torch.bfloat16).pin_memory()
+        self.workspace = nat.AttentionWorkspace(num_seqs, hkv, device=eng.device)
+        self.num_pairs = 0
+
+    def field(self, name: str, rows: int | None = None) -> torch.Tensor:
+        """Typed view of one input inside the pinned packed buffer."""
+        shape = list(self.shapes[name])
+        if rows is not None:
+            shape[0] = rows
+        dt = self._DTYPES[name]
+        n = int(np.prod(shape)) * torch.tensor([], dtype=dt).element_size()
+        off = self.layout[name]
+        return self.host[off: off + n].view(dt).view(shape)
+
+    def pack(self, q, k, v, slots, tables, ctx, pairs=None) -> int:
+        """Copy a step's inputs (CPU tensors) into the packed buffer; returns
+        its size in bytes for this number of pairs."""
+        self.field("q").copy_(q)
+        self.field("k_new").copy_(k)
+        self.field("v_new").copy_(v)
+        self.field("slot_mapping").copy_(torch.as_tensor(slots, dtype=torch.int64))
+        self.field("block_tables").copy_(tables)
+        self.field("context_lens").copy_(ctx)
+        n = 0 if pairs is None else int(len(pairs))
+        if n > self.max_pairs:
+            raise ValueError(f"{n} copy pairs exceed the buffer's {self.max_pairs}")
+        if n:
+            self.field("src_dst_pairs", n).copy_(torch.as_tensor(pairs, dtype=torch.int32).reshape(n, 2))
+        self.num_pairs = n
+        return nat.step_layout(self.num_seqs, self.eng.num_q_heads, self.eng.num_kv_heads, self.eng.head_dim,
+                               self.width, n)["bytes"]
+
+    def run(self, scale: float, num_ctas: int = 0, stream=None) -> torch.Tensor:
+        """Enqueue the step; out_host holds the output once the stream passes it."""
+        e = self.eng
+        nat.decode_step_host(self.host, self.staging, self.num_pairs, e.k_cache, e.v_cache, self.width,
+                             self.num_seqs, e.num_q_heads, scale, self.workspace, self.out_dev, self.out_host,
+                             e.error, num_ctas, stream)
+        return self.out_host

@@ -62,3 +62,24 @@ def test_host_argument_checks_need_no_gpu(lib_path):
     assert h is not None
     L.pkv_bm_destroy(h)
     assert L.pkv_attn_decode_ex(None, None, None, None, 1, None, 1, 32, 8, 128, 1, 16, 1.0, 0, None, 0, None, None) == nat.PKV_EINVAL
+
+
+def test_step_layout_is_packed_and_aligned(lib_path):
+    import paged_kv_cache_49_gb300._native as nat
+    B, hq, hkv, d, w = 5, 32, 8, 128, 37
+    order = ["q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens", "src_dst_pairs"]
+    sizes = {"q": B * hq * d * 2, "k_new": B * hkv * d * 2, "v_new": B * hkv * d * 2, "slot_mapping": B * 8,
+             "block_tables": B * w * 4, "context_lens": B * 4}
+    for pairs in (0, 3):
+        lay = nat.step_layout(B, hq, hkv, d, w, pairs)
+        sizes["src_dst_pairs"] = pairs * 8
+        end = 0
+        for name in order:
+            assert lay[name] % 256 == 0 and lay[name] >= end
+            end = lay[name] + sizes[name]
+        assert lay["bytes"] >= end and lay["bytes"] - end < 256
+    assert nat.step_layout(B, hq, hkv, d, w, 0)["context_lens"] == nat.step_layout(B, hq, hkv, d, w, 9)["context_lens"]
+    lay = nat.StepLayoutT()
+    assert nat.lib.pkv_step_layout(0, 32, 8, 128, 1, 0, ctypes.byref(lay)) == nat.PKV_EINVAL
+    assert nat.lib.pkv_decode_step_host(None, None, 0, None, None, 1, 1, 1, 32, 8, 128, 1.0, 0, None, 0, None,
+                                        None, None, None) == nat.PKV_EINVAL
