@@ -136,13 +136,15 @@ __device__ __forceinline__ int find_seq(const int* scan, int n, int t) {
     return lo;
 }
 
-__device__ __forceinline__ Cursor locate(const int* scan, int n, int hkv, long long x) {
+// Positions on the line are 32-bit: the host rejects launches whose line
+// could reach 2^30 tiles.
+__device__ __forceinline__ Cursor locate(const int* scan, int n, int hkv, int x) {
     Cursor c;
-    c.s = find_seq(scan, n, static_cast<int>(x / hkv));
+    c.s = find_seq(scan, n, x / hkv);
     const int nb = run_blocks(scan, c.s);
-    const long long off = x - static_cast<long long>(hkv) * (scan[c.s] - nb);
-    c.g = static_cast<int>(off / nb);
-    c.blk = static_cast<int>(off % nb);
+    const int off = x - hkv * (scan[c.s] - nb);
+    c.g = off / nb;
+    c.blk = off - c.g * nb;
     return c;
 }
 
@@ -166,7 +168,7 @@ __device__ __forceinline__ int clamped_ctx(const Params& p, int s) {
 // whose run has nb blocks; start = its position on the line.
 struct Piece {
     int s, g, blk, nb, len;
-    long long start;
+    int start;
 };
 
 // The pieces of one CTA's range in processing order: the range's last piece
@@ -177,15 +179,15 @@ struct Piece {
 struct PieceWalk {
     const int* scan;
     int n, hkv;
-    long long range_lo, split, x, end;
+    int range_lo, split, x, end;
     int part;
     Cursor c;
 
-    __device__ PieceWalk(const int* scan_, int n_, int hkv_, long long lo, long long hi)
+    __device__ PieceWalk(const int* scan_, int n_, int hkv_, int lo, int hi)
         : scan(scan_), n(n_), hkv(hkv_), range_lo(lo), part(0) {
         const Cursor last = locate(scan, n, hkv, hi - 1);
         const int nb = run_blocks(scan, last.s);
-        const long long seg = static_cast<long long>(hkv) * (scan[last.s] - nb) + static_cast<long long>(last.g) * nb;
+        const int seg = hkv * (scan[last.s] - nb) + last.g * nb;
         split = seg > lo ? seg : lo;
         x = split;
         end = hi;
@@ -205,7 +207,7 @@ struct PieceWalk {
         pc.g = c.g;
         pc.blk = c.blk;
         pc.nb = nb;
-        pc.len = static_cast<int>(min(static_cast<long long>(nb - c.blk), end - x));
+        pc.len = min(nb - c.blk, end - x);
         pc.start = x;
         advance(c, scan, n, hkv, pc.len);
         x += pc.len;
@@ -296,19 +298,20 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         __syncthreads();
     }
 
-    const long long total = static_cast<long long>(Hkv) * scan[B - 1];
-    const long long chunk = (total + gridDim.x - 1) / gridDim.x;
-    const long long range_lo = min(total, static_cast<long long>(blockIdx.x) * chunk);
-    const long long range_hi = min(total, range_lo + chunk);
+    const int total = Hkv * scan[B - 1];
+    const int chunk = (total + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
+    const int range_lo = static_cast<int>(min(static_cast<long long>(total), static_cast<long long>(blockIdx.x) * chunk));
+    const int range_hi = range_lo + min(chunk, total - range_lo);
 
-    // Warm L2 with the block-table entries and query rows of every piece of
-    // this CTA's range, so that the producer's reads of them later on are
-    // L2 hits rather than dependent DRAM round trips.
-    if (warp == kProducerWarp && range_lo < range_hi) {
+    // The merge warp, idle until the first piece ends, warms L2 with the
+    // block-table entries and query rows of every piece of this CTA's range,
+    // so that the producer's reads of them after its first piece are L2 hits
+    // rather than dependent DRAM round trips.
+    if (warp == kMergeWarp && range_lo < range_hi) {
         Cursor c = locate(scan, B, Hkv, range_lo);
-        for (long long xx = range_lo; xx < range_hi;) {
+        for (int xx = range_lo; xx < range_hi;) {
             const int nb = run_blocks(scan, c.s);
-            const int len = static_cast<int>(min(static_cast<long long>(nb - c.blk), range_hi - xx));
+            const int len = min(nb - c.blk, range_hi - xx);
             const int e0 = c.blk * kTok / kBT, e1 = ((c.blk + len) * kTok + kBT - 1) / kBT;
             const int32_t* t0 = p.block_tables + static_cast<size_t>(c.s) * p.max_blocks + e0;
             const char* t1 = reinterpret_cast<const char*>(t0 + (e1 - e0));
@@ -323,9 +326,13 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     }
 
     // Everything above reads only inputs that the kernels of a decode step
-    // (block copy, append) do not write; from here on the kernel may touch
-    // what they wrote (the KV cache), so wait for them when launched early.
-    griddep_wait();
+    // (block copy, append) do not write. Of what follows, only the
+    // producer's tile loads read what they wrote (the KV cache): the producer
+    // reads its first piece's query rows and table entries first, then waits
+    // for those kernels (when launched early) just before its first tile
+    // load. Every other thread waits here, so that the grid never completes
+    // before the kernels it was launched behind.
+    if (warp != kProducerWarp) griddep_wait();
 
     // Sequences with no context get a zero output row (CTA 0, merge warp).
     if (blockIdx.x == 0 && warp == kMergeWarp) {
@@ -336,7 +343,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             for (int i = lane; i < row_vec; i += 32) dst[i] = make_uint4(0, 0, 0, 0);
         }
     }
-    if (range_lo >= range_hi) return;
+    if (range_lo >= range_hi) {
+        if (warp == kProducerWarp) griddep_wait();
+        return;
+    }
 
     if (warp == kProducerWarp) {
         // ======================= producer warp =======================
@@ -345,8 +355,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         Piece pc;
         int stage = 0, qslot = 0;
         uint32_t sphase = 0, qphase = 0;
-        long long issued = 0;
+        int issued = 0;
         int q_issued = 0;
+        bool waited = false;  // griddep_wait done by this thread
         while (walk.next(pc)) {
             const int len = pc.len;
             if (lane == 0) {
@@ -387,6 +398,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                     const int ya = __shfl_sync(0xffffffffu, y0, jj);
                     const int yb = __shfl_sync(0xffffffffu, y1, jj);
                     if (lane == 0) {
+                        if (!waited) {
+                            griddep_wait();
+                            waited = true;
+                        }
                         if (mbar_wait(empty_bar(stage), sphase ^ 1u, abort_flag, p.err)) {
                             const uint32_t fb = full_bar(stage);
                             mbar_arrive_expect_tx(fb, kStageBytes);
@@ -418,9 +433,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         // copies it issued that may still be in flight, so that no TMA lands in
         // shared memory after the CTA has exited. Copies were issued in order,
         // so those are at most the last kStages blocks and kQSlots query loads.
+        if (!waited) griddep_wait();
         if (lane == 0) {
             volatile int never = 0;
-            for (long long i = max(0ll, issued - kStages); i < issued; ++i)
+            for (int i = max(0, issued - kStages); i < issued; ++i)
                 mbar_wait(full_bar(static_cast<int>(i % kStages)),
                           static_cast<uint32_t>((i / kStages) & 1), &never, nullptr);
             for (int i = max(0, q_issued - kQSlots); i < q_issued; ++i)
@@ -439,7 +455,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         int piece = 0;
         while (walk.next(pc)) {
             const int s = pc.s, g = pc.g, nb = pc.nb;
-            const long long seg_start = static_cast<long long>(Hkv) * (scan[s] - nb) + static_cast<long long>(g) * nb;
+            const int seg_start = Hkv * (scan[s] - nb) + g * nb;
             const int i0 = static_cast<int>(seg_start / chunk);
             const int i1 = static_cast<int>((seg_start + nb - 1) / chunk);
             const int pieces = i1 - i0 + 1;
@@ -482,14 +498,16 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             }
             mbar_arrive(mempty_bar(ms));  // the consumers may reuse this slot
             if (pieces > 1) {
-                __threadfence();
+                // Publish this piece's partial (every lane's stores, ordered
+                // before lane 0's release by the warp barrier) and count it;
+                // the last piece of the pair to arrive acquires the others'.
                 __syncwarp();
                 int old = 0;
-                if (lane == 0) old = atomicAdd(p.counters + s * Hkv + g, 1);
+                if (lane == 0) old = atom_add_acq_rel_gpu(p.counters + s * Hkv + g, 1);
                 old = __shfl_sync(0xffffffffu, old, 0);
+                __syncwarp();
                 if (old == pieces - 1) {  // last piece of the pair to finish: merge them all
-                    __threadfence();
-                    const int slot0 = (seg_start == static_cast<long long>(i0) * chunk) ? 0 : 1;
+                    const int slot0 = (seg_start == i0 * chunk) ? 0 : 1;
                     // One online log-sum-exp pass over the pieces; for each
                     // piece the loads of every head are issued together.
                     float Mr[kMaxG], Lr[kMaxG];
@@ -559,7 +577,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
 
     PieceWalk walk(scan, B, Hkv, range_lo, range_hi);
     Piece pc;
-    long long gidx0 = 0;
+    int gidx0 = 0;
     int qslot = 0, piece = 0;
     uint32_t qphase = 0;
     while (walk.next(pc)) {
@@ -594,7 +612,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         // would then see the previous phase's parity and pass too early.
         for (int jb = (warp - static_cast<int>(gidx0 % kConsumerWarps)) & (kConsumerWarps - 1); jb < len;
              jb += kConsumerWarps) {
-            const long long gi = gidx0 + jb;
+            const int gi = gidx0 + jb;
             const int st = static_cast<int>(gi % kStages);
             mbar_wait(full_bar(st), static_cast<uint32_t>((gi / kStages) & 1), abort_flag, p.err);
             const int valid = (blk0 + jb == nb - 1) ? ctx - kTok * (nb - 1) : kTok;
@@ -825,7 +843,7 @@ pkv_status prepare(const void* q, const void* k_cache, const void* v_cache, cons
     if (static_cast<long long>(num_blocks) * num_kv_heads * block_tokens >= (1ll << 31) ||
         static_cast<long long>(num_seqs) * max_blocks_per_seq >= (1ll << 31) ||
         static_cast<long long>(max_blocks_per_seq) * block_tokens >= (1ll << 31) ||
-        static_cast<long long>(num_kv_heads) * num_seqs * max_blocks_per_seq * block_tokens / kTok >= (1ll << 31))
+        static_cast<long long>(num_kv_heads) * num_seqs * max_blocks_per_seq * block_tokens / kTok >= (1ll << 30))
         return PKV_ERANGE;
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
         (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
@@ -1149,7 +1167,7 @@ extern "C" pkv_status pkv_attn_decode_static(const void* q, const void* k_cache,
     if (static_cast<long long>(num_blocks) * num_kv_heads * PKV_BLOCK_TOKENS >= (1ll << 31) ||
         static_cast<long long>(num_seqs) * max_blocks_per_seq >= (1ll << 31) ||
         static_cast<long long>(max_blocks_per_seq) * PKV_BLOCK_TOKENS >= (1ll << 31) ||
-        static_cast<long long>(num_kv_heads) * num_seqs * max_blocks_per_seq >= (1ll << 31))
+        static_cast<long long>(num_kv_heads) * num_seqs * max_blocks_per_seq >= (1ll << 30))
         return PKV_ERANGE;
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return PKV_EINVAL;
     const int auto_grid = attn::grid_for(num_seqs);

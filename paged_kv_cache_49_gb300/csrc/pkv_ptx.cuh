@@ -18,6 +18,16 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     return t;
 }
 
+// Atomic add at GPU scope with acquire-release semantics: the caller's earlier
+// writes (and, after a __syncwarp, its warp's) are visible to whoever
+// acquires the updated value, and the caller's later reads see every write
+// released by earlier adders.
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int* addr, int v) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
+    return old;
+}
+
 // ---- mbarrier ----------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
