@@ -508,8 +508,11 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 __syncwarp();
                 if (old == pieces - 1) {  // last piece of the pair to finish: merge them all
                     const int slot0 = (seg_start == i0 * chunk) ? 0 : 1;
-                    // One online log-sum-exp pass over the pieces; for each
-                    // piece the loads of every head are issued together.
+                    // An online log-sum-exp pass over the pieces, four pieces
+                    // (and four heads) at a time: each batch's loads are all
+                    // issued before any of them is used, so a pair split into
+                    // P pieces costs about P / 4 round trips to L2 (twice
+                    // that for groups of more than four heads), not P.
                     float Mr[kMaxG], Lr[kMaxG];
                     float4 Ar[kMaxG];
 #pragma unroll
@@ -518,29 +521,53 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                         Lr[h] = 0.f;
                         Ar[h] = make_float4(0.f, 0.f, 0.f, 0.f);
                     }
-                    for (int i = i0; i <= i1; ++i) {
-                        const float* pi = p.partials + (static_cast<size_t>(i) * 2 + (i == i0 ? slot0 : 0)) * kPartialFloats;
-                        float mi[kMaxG], li[kMaxG];
-                        float4 oi[kMaxG];
+                    for (int i = i0; i <= i1; i += 4) {
 #pragma unroll
-                        for (int h = 0; h < kMaxG; ++h) {
-                            if (h < G) {
-                                mi[h] = __ldcg(pi + h * kORow + kDim);
-                                li[h] = __ldcg(pi + h * kORow + kDim + 1);
-                                oi[h] = __ldcg(reinterpret_cast<const float4*>(pi + h * kORow + d0));
-                            }
-                        }
+                        for (int hb = 0; hb < kMaxG; hb += 4) {
+                            if (hb < G) {
+                                float mk[4][4], lk[4][4];
+                                float4 ok[4][4];
 #pragma unroll
-                        for (int h = 0; h < kMaxG; ++h) {
-                            if (h < G) {
-                                const float mn = fmaxf(Mr[h], mi[h]);
-                                const float a = ex2(Mr[h] - mn), b = ex2(mi[h] - mn);
-                                Lr[h] = Lr[h] * a + li[h] * b;
-                                Ar[h].x = Ar[h].x * a + oi[h].x * b;
-                                Ar[h].y = Ar[h].y * a + oi[h].y * b;
-                                Ar[h].z = Ar[h].z * a + oi[h].z * b;
-                                Ar[h].w = Ar[h].w * a + oi[h].w * b;
-                                Mr[h] = mn;
+                                for (int k = 0; k < 4; ++k) {
+                                    const float* pi = p.partials +
+                                        (static_cast<size_t>(i + k) * 2 + (i + k == i0 ? slot0 : 0)) * kPartialFloats;
+#pragma unroll
+                                    for (int h = 0; h < 4; ++h) {
+                                        if (i + k <= i1 && hb + h < G) {
+                                            mk[k][h] = __ldcg(pi + (hb + h) * kORow + kDim);
+                                            lk[k][h] = __ldcg(pi + (hb + h) * kORow + kDim + 1);
+                                            ok[k][h] = __ldcg(reinterpret_cast<const float4*>(pi + (hb + h) * kORow + d0));
+                                        } else {
+                                            mk[k][h] = NEG_INF;
+                                            lk[k][h] = 0.f;
+                                            ok[k][h] = make_float4(0.f, 0.f, 0.f, 0.f);
+                                        }
+                                    }
+                                }
+#pragma unroll
+                                for (int h = 0; h < 4; ++h) {
+                                    const int H = hb + h;
+                                    if (H < G) {
+                                        float mn = Mr[H];
+#pragma unroll
+                                        for (int k = 0; k < 4; ++k) mn = fmaxf(mn, mk[k][h]);
+                                        const float a = ex2(Mr[H] - mn);
+                                        float L = Lr[H] * a;
+                                        float4 A = make_float4(Ar[H].x * a, Ar[H].y * a, Ar[H].z * a, Ar[H].w * a);
+#pragma unroll
+                                        for (int k = 0; k < 4; ++k) {
+                                            const float b = ex2(mk[k][h] - mn);  // 0 for absent pieces
+                                            L += b * lk[k][h];
+                                            A.x += b * ok[k][h].x;
+                                            A.y += b * ok[k][h].y;
+                                            A.z += b * ok[k][h].z;
+                                            A.w += b * ok[k][h].w;
+                                        }
+                                        Mr[H] = mn;
+                                        Lr[H] = L;
+                                        Ar[H] = A;
+                                    }
+                                }
                             }
                         }
                     }
