@@ -88,7 +88,9 @@ constexpr int kNumBars = 2 * kStages + 2 * kQSlots + 2 * kMergeSlots;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kOffScan = kOffMisc + 64;
 
-constexpr size_t smem_bytes(int num_seqs) { return 1024 + kOffScan + 4 * static_cast<size_t>(num_seqs); }
+// Dynamic shared memory: the fixed part, the prefix sum (4 bytes per
+// sequence) and each sequence's last-tile token count (1 byte per sequence).
+constexpr size_t smem_bytes(int num_seqs) { return 1024 + kOffScan + 5 * static_cast<size_t>(num_seqs); }
 
 constexpr size_t kWsHeader = 256;
 
@@ -232,6 +234,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     const int G = p.group;
 
     int* scan = reinterpret_cast<int*>(smem + kOffScan);
+    uint8_t* tail = smem + kOffScan + 4 * static_cast<size_t>(B);  // tokens in each sequence's last tile
     int* misc = reinterpret_cast<int*>(smem + kOffMisc);
     volatile int* abort_flag = misc;  // misc[0]
     int* warp_tot = misc + 8;         // misc[8 .. 8 + kThreads / 32)
@@ -292,8 +295,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         for (int w = 0; w < warp; ++w) run += warp_tot[w];
         for (int s = lo; s < hi; ++s) {
             const int cc = clamped_ctx(p, s);
-            run += cc > 0 ? (cc + kTok - 1) / kTok : 0;
+            const int tiles = cc > 0 ? (cc + kTok - 1) / kTok : 0;
+            run += tiles;
             scan[s] = run;
+            tail[s] = static_cast<uint8_t>(cc - kTok * (tiles - 1));  // 1..16 (unused when tiles == 0)
         }
         __syncthreads();
     }
@@ -304,25 +309,27 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     const int range_hi = range_lo + min(chunk, total - range_lo);
 
     // The merge warp, idle until the first piece ends, warms L2 with the
-    // block-table entries and query rows of every piece of this CTA's range,
-    // so that the producer's reads of them after its first piece are L2 hits
-    // rather than dependent DRAM round trips.
+    // block-table entries and query rows of this CTA's range -- two
+    // contiguous spans, from the range's first tile to its last, each capped
+    // at kWarmBytes -- so that the producer's reads of them after its first
+    // piece are L2 hits rather than dependent DRAM round trips.
     if (warp == kMergeWarp && range_lo < range_hi) {
-        Cursor c = locate(scan, B, Hkv, range_lo);
-        for (int xx = range_lo; xx < range_hi;) {
-            const int nb = run_blocks(scan, c.s);
-            const int len = min(nb - c.blk, range_hi - xx);
-            const int e0 = c.blk * kTok / kBT, e1 = ((c.blk + len) * kTok + kBT - 1) / kBT;
-            const int32_t* t0 = p.block_tables + static_cast<size_t>(c.s) * p.max_blocks + e0;
-            const char* t1 = reinterpret_cast<const char*>(t0 + (e1 - e0));
-            const char* line = reinterpret_cast<const char*>(reinterpret_cast<uintptr_t>(t0) & ~uintptr_t(127));
-            for (const char* a = line + lane * 128; a < t1; a += 32 * 128) prefetch_l2(a);
-            const char* qrow = reinterpret_cast<const char*>(
-                p.q + (static_cast<size_t>(c.s) * p.num_q_heads + static_cast<size_t>(c.g) * G) * kDim);
-            if (lane < G * 2) prefetch_l2(qrow + lane * 128);
-            advance(c, scan, B, Hkv, len);
-            xx += len;
-        }
+        constexpr size_t kWarmBytes = 256 * 1024;
+        const Cursor a = locate(scan, B, Hkv, range_lo);
+        const Cursor z = locate(scan, B, Hkv, range_hi - 1);
+        auto warm = [&](const char* lo, const char* hi) {
+            if (hi - lo > static_cast<ptrdiff_t>(kWarmBytes)) hi = lo + kWarmBytes;
+            const char* line = reinterpret_cast<const char*>(reinterpret_cast<uintptr_t>(lo) & ~uintptr_t(127));
+            for (const char* x = line + lane * 128; x < hi; x += 32 * 128) prefetch_l2(x);
+        };
+        warm(reinterpret_cast<const char*>(p.block_tables + static_cast<size_t>(a.s) * p.max_blocks +
+                                           a.blk * kTok / kBT),
+             reinterpret_cast<const char*>(p.block_tables + static_cast<size_t>(z.s) * p.max_blocks +
+                                           ((z.blk + 1) * kTok + kBT - 1) / kBT));
+        warm(reinterpret_cast<const char*>(p.q + (static_cast<size_t>(a.s) * p.num_q_heads +
+                                                  static_cast<size_t>(a.g) * G) * kDim),
+             reinterpret_cast<const char*>(p.q + (static_cast<size_t>(z.s) * p.num_q_heads +
+                                                  static_cast<size_t>(z.g + 1) * G) * kDim));
     }
 
     // Everything above reads only inputs that the kernels of a decode step
@@ -334,10 +341,11 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     // before the kernels it was launched behind.
     if (warp != kProducerWarp) griddep_wait();
 
-    // Sequences with no context get a zero output row (CTA 0, merge warp).
-    if (blockIdx.x == 0 && warp == kMergeWarp) {
+    // Sequences with no context get a zero output row (sequence s by CTA
+    // s mod gridDim.x, merge warp).
+    if (warp == kMergeWarp) {
         const int row_vec = p.num_q_heads * kDim / 8;
-        for (int s = 0; s < B; ++s) {
+        for (int s = blockIdx.x; s < B; s += gridDim.x) {
             if (run_blocks(scan, s) != 0) continue;
             uint4* dst = reinterpret_cast<uint4*>(p.out + static_cast<size_t>(s) * p.num_q_heads * kDim);
             for (int i = lane; i < row_vec; i += 32) dst[i] = make_uint4(0, 0, 0, 0);
@@ -371,7 +379,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             }
             if (++qslot == kQSlots) { qslot = 0; qphase ^= 1u; }
             const int32_t* row = p.block_tables + static_cast<size_t>(pc.s) * p.max_blocks;
-            const int seq_blocks = (clamped_ctx(p, pc.s) + kBT - 1) / kBT;  // valid table entries
+            const int seq_blocks = (kTok * (pc.nb - 1) + tail[pc.s] + kBT - 1) / kBT;  // valid table entries
             auto block_id = [&](int e) {
                 int bid = __ldg(row + e);
                 if (bid < 0 || bid >= p.num_blocks) {
@@ -609,7 +617,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     uint32_t qphase = 0;
     while (walk.next(pc)) {
         const int s = pc.s, blk0 = pc.blk, nb = pc.nb, len = pc.len;
-        const int ctx = clamped_ctx(p, s);
+        const int last_valid = tail[s];  // tokens in the run's last tile
 
         // ---- query fragments (B operand of S^T = K Q^T) ----
         uint32_t qb[16];
@@ -642,7 +650,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             const int gi = gidx0 + jb;
             const int st = static_cast<int>(gi % kStages);
             mbar_wait(full_bar(st), static_cast<uint32_t>((gi / kStages) & 1), abort_flag, p.err);
-            const int valid = (blk0 + jb == nb - 1) ? ctx - kTok * (nb - 1) : kTok;
+            const int valid = (blk0 + jb == nb - 1) ? last_valid : kTok;
             const uint32_t sk = stage_base + st * kStageBytes;
             const uint32_t sv = sk + kBlockBytes;
 

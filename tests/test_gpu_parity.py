@@ -78,6 +78,26 @@ def test_small_workloads_all_splits(pkv, name):
     _run_workload(pkv, w, num_ctas_list=(0, 1, 2, 3, 7, 37, 151))
 
 
+@pytest.mark.parametrize("name", ["heads_8_8", "heads_16_8", "heads_8_1", "heads_64_8"])
+def test_gqa_group_sizes(pkv, name):
+    """G = 1 (MHA), 2, 8 with a single KV head (MQA) and 8 with eight."""
+    w = make_workload(name)
+    _run_workload(pkv, w, num_ctas_list=(0, 1, 5, 40))
+
+
+def test_long_single_sequence_merges_across_every_cta(pkv):
+    """One 131,072-token sequence: each KV head's run is cut among ~38 CTAs,
+    so the last arrival merges dozens of partials."""
+    w = make_workload("long_single")
+    _run_workload(pkv, w, num_ctas_list=(0, 7))
+
+
+def test_many_short_sequences_at_the_batch_limit(pkv):
+    """4,096 sequences of 1..40 tokens: thousands of short pieces per launch."""
+    w = make_workload("many_short")
+    _run_workload(pkv, w, num_ctas_list=(0, 33))
+
+
 def test_llama3_8b_batch64(pkv):
     w = make_workload("llama3_8b_b64")
     _run_workload(pkv, w, num_ctas_list=(0, 1, 64))

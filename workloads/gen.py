@@ -263,7 +263,34 @@ def fanout(seed: int = 0, prompts: int = 16, samples: int = 8) -> Workload:
     return w
 
 
+def heads(seed: int = 0, hq: int = 8, hkv: int = 8) -> Workload:
+    """Edge shapes of the GQA mapping: MHA (G = 1), G = 2, MQA (one KV head),
+    on a small ragged batch that spans several blocks and a partial tail."""
+    return _decode_batch(f"heads_{hq}_{hkv}", f"batch 6, ctx mix, {hq} q / {hkv} kv heads", seed, hq, hkv,
+                         [1, 15, 16, 33, 200, 517])
+
+
+def long_single(seed: int = 0) -> Workload:
+    """One 131,072-token sequence with the 70B geometry: every CTA holds a
+    piece of the same (sequence, KV head) runs, so the merge spans many CTAs."""
+    return _decode_batch("long_single", "batch 1, ctx 131072, 64 q / 8 kv heads", seed, 64, 8, [131072])
+
+
+def many_short(seed: int = 0) -> Workload:
+    """The largest batch the kernel takes (4,096 sequences), 1..40 tokens each:
+    thousands of short runs and pieces per CTA."""
+    r = _rng(seed, _TAG_PARAMS, 0)
+    ctx = r.integers(1, 41, size=4096)
+    return _decode_batch("many_short", "batch 4096, ctx U[1, 40], 32 q / 8 kv heads", seed, 32, 8, ctx)
+
+
 WORKLOADS = {
+    "heads_8_8": lambda seed=0: heads(seed, 8, 8),
+    "heads_16_8": lambda seed=0: heads(seed, 16, 8),
+    "heads_8_1": lambda seed=0: heads(seed, 8, 1),
+    "heads_64_8": lambda seed=0: heads(seed, 64, 8),
+    "long_single": long_single,
+    "many_short": many_short,
     "tiny": tiny,
     "tiny_nan": tiny_nan,
     "llama3_8b_b64": llama3_8b,
