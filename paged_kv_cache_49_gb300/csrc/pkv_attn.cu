@@ -368,16 +368,18 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         bool waited = false;  // griddep_wait done by this thread
         while (walk.next(pc)) {
             const int len = pc.len;
-            if (lane == 0) {
-                if (mbar_wait(qempty_bar(qslot), qphase ^ 1u, abort_flag, p.err)) {
-                    mbar_arrive_expect_tx(qfull_bar(qslot), G * kDim * 2);
-                    const __nv_bfloat16* src =
-                        p.q + (static_cast<size_t>(pc.s) * p.num_q_heads + static_cast<size_t>(pc.g) * G) * kDim;
-                    bulk_load(smem_u32(smem + kOffQ + qslot * kQBytes), src, G * kDim * 2, qfull_bar(qslot));
-                    ++q_issued;
+            if (len >= kConsumerWarps) {  // short pieces: the consumers read their query rows themselves
+                if (lane == 0) {
+                    if (mbar_wait(qempty_bar(qslot), qphase ^ 1u, abort_flag, p.err)) {
+                        mbar_arrive_expect_tx(qfull_bar(qslot), G * kDim * 2);
+                        const __nv_bfloat16* src =
+                            p.q + (static_cast<size_t>(pc.s) * p.num_q_heads + static_cast<size_t>(pc.g) * G) * kDim;
+                        bulk_load(smem_u32(smem + kOffQ + qslot * kQBytes), src, G * kDim * 2, qfull_bar(qslot));
+                        ++q_issued;
+                    }
                 }
+                if (++qslot == kQSlots) { qslot = 0; qphase ^= 1u; }
             }
-            if (++qslot == kQSlots) { qslot = 0; qphase ^= 1u; }
             const int32_t* row = p.block_tables + static_cast<size_t>(pc.s) * p.max_blocks;
             const int seq_blocks = (kTok * (pc.nb - 1) + tail[pc.s] + kBT - 1) / kBT;  // valid table entries
             auto block_id = [&](int e) {
@@ -461,46 +463,83 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         PieceWalk walk(scan, B, Hkv, range_lo, range_hi);
         Piece pc;
         int piece = 0;
+        int gidx0 = 0;  // the CTA's block count before this piece, as the consumers count it
         while (walk.next(pc)) {
             const int s = pc.s, g = pc.g, nb = pc.nb;
+            // consumer warps that hold blocks of this piece (all of them unless it is short)
+            unsigned owners = 0;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w)
+                if (((w - gidx0 % kConsumerWarps) & (kConsumerWarps - 1)) < pc.len) owners |= 1u << w;
+            gidx0 += pc.len;
             const int seg_start = Hkv * (scan[s] - nb) + g * nb;
             const int i0 = static_cast<int>(seg_start / chunk);
             const int i1 = static_cast<int>((seg_start + nb - 1) / chunk);
             const int pieces = i1 - i0 + 1;
-            const int ms = piece & 1;
-            mbar_wait(mfull_bar(ms), static_cast<uint32_t>((piece >> 1) & 1), abort_flag, p.err);
+            const int ms = piece % kMergeSlots;
+            mbar_wait(mfull_bar(ms), static_cast<uint32_t>((piece / kMergeSlots) & 1), abort_flag, p.err);
             const float* mo = sm_o + ms * kMergeOFloats;
             const float* mm = sm_m + ms * kMergeMLFloats;
             const float* ml = sm_l + ms * kMergeMLFloats;
             __nv_bfloat16* out_base =
                 p.out + (static_cast<size_t>(s) * p.num_q_heads + static_cast<size_t>(g) * G) * kDim + d0;
             float* part = p.partials + (static_cast<size_t>(blockIdx.x) * 2 + (pc.start == range_lo ? 0 : 1)) * kPartialFloats;
-            for (int h = 0; h < G; ++h) {
-                float M = NEG_INF;
+            // Four heads at a time: every shared-memory read of the four
+            // heads' warp states is issued before any of them is used.
 #pragma unroll
-                for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mm[w * kMaxG + h]);
-                float L = 0.f;
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int hb = 0; hb < kMaxG; hb += 4) {
+                if (hb < G) {
+                    float mk[kConsumerWarps][4], lk[kConsumerWarps][4];
+                    float4 ok[kConsumerWarps][4];
 #pragma unroll
-                for (int w = 0; w < kConsumerWarps; ++w) {
-                    const float mw = mm[w * kMaxG + h];
-                    if (mw == NEG_INF) continue;  // this warp got no block of the piece
-                    const float f = ex2(mw - M);
-                    L += f * ml[w * kMaxG + h];
-                    const float4 u = *reinterpret_cast<const float4*>(mo + (w * kMaxG + h) * kORow + d0);
-                    acc.x += f * u.x; acc.y += f * u.y; acc.z += f * u.z; acc.w += f * u.w;
-                }
-                if (pieces == 1) {
-                    const float inv = 1.f / L;
-                    uint2 w2;
-                    w2.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-                    w2.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-                    *reinterpret_cast<uint2*>(out_base + static_cast<size_t>(h) * kDim) = w2;
-                } else {
-                    *reinterpret_cast<float4*>(part + h * kORow + d0) = acc;
-                    if (lane == 0) {
-                        part[h * kORow + kDim] = M;
-                        part[h * kORow + kDim + 1] = L;
+                    for (int w = 0; w < kConsumerWarps; ++w) {
+#pragma unroll
+                        for (int hh = 0; hh < 4; ++hh) {
+                            const int h = hb + hh;
+                            if (((owners >> w) & 1u) && h < G) {  // warps without blocks of the piece wrote nothing
+                                mk[w][hh] = mm[w * kMaxG + h];
+                                lk[w][hh] = ml[w * kMaxG + h];
+                                ok[w][hh] = *reinterpret_cast<const float4*>(mo + (w * kMaxG + h) * kORow + d0);
+                            } else {
+                                mk[w][hh] = NEG_INF;
+                                lk[w][hh] = 0.f;
+                                ok[w][hh] = make_float4(0.f, 0.f, 0.f, 0.f);
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int hh = 0; hh < 4; ++hh) {
+                        const int h = hb + hh;
+                        if (h < G) {
+                            float M = NEG_INF;
+#pragma unroll
+                            for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mk[w][hh]);
+                            float L = 0.f;
+                            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                            for (int w = 0; w < kConsumerWarps; ++w) {
+                                if (!((owners >> w) & 1u)) continue;
+                                const float f = ex2(mk[w][hh] - M);
+                                L += f * lk[w][hh];
+                                acc.x += f * ok[w][hh].x;
+                                acc.y += f * ok[w][hh].y;
+                                acc.z += f * ok[w][hh].z;
+                                acc.w += f * ok[w][hh].w;
+                            }
+                            if (pieces == 1) {
+                                const float inv = 1.f / L;
+                                uint2 w2;
+                                w2.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+                                w2.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+                                *reinterpret_cast<uint2*>(out_base + static_cast<size_t>(h) * kDim) = w2;
+                            } else {
+                                *reinterpret_cast<float4*>(part + h * kORow + d0) = acc;
+                                if (lane == 0) {
+                                    part[h * kORow + kDim] = M;
+                                    part[h * kORow + kDim + 1] = L;
+                                }
+                            }
+                        }
                     }
                 }
             }
@@ -618,21 +657,37 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     while (walk.next(pc)) {
         const int s = pc.s, blk0 = pc.blk, nb = pc.nb, len = pc.len;
         const int last_valid = tail[s];  // tokens in the run's last tile
+        // A piece shorter than the consumer warp count has blocks for some
+        // warps only; the others skip it but for the merge-slot handshake.
+        const int first = (warp - static_cast<int>(gidx0 % kConsumerWarps)) & (kConsumerWarps - 1);
+        const bool mine = first < len;
 
         // ---- query fragments (B operand of S^T = K Q^T) ----
+        // Full pieces: from the shared-memory ring the producer fills. Short
+        // pieces: each warp that has a block reads its fragments straight
+        // from global memory (L2-warm), so that no warp waits on a query copy
+        // for a piece it takes no part in.
         uint32_t qb[16];
-        mbar_wait(qfull_bar(qslot), qphase, abort_flag, p.err);
-        {
+        if (len >= kConsumerWarps) {
+            mbar_wait(qfull_bar(qslot), qphase, abort_flag, p.err);
             const uint8_t* qs = smem + kOffQ + qslot * kQBytes + r * (kDim * 2) + c * 4;
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
                 qb[2 * ks] = r < G ? *reinterpret_cast<const uint32_t*>(qs + ks * 32) : 0u;
                 qb[2 * ks + 1] = r < G ? *reinterpret_cast<const uint32_t*>(qs + ks * 32 + 16) : 0u;
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(qempty_bar(qslot));
+            if (++qslot == kQSlots) { qslot = 0; qphase ^= 1u; }
+        } else if (mine) {
+            const uint32_t* qg = reinterpret_cast<const uint32_t*>(
+                p.q + (static_cast<size_t>(s) * p.num_q_heads + static_cast<size_t>(pc.g) * G + r) * kDim) + c;
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                qb[2 * ks] = r < G ? __ldg(qg + ks * 8) : 0u;
+                qb[2 * ks + 1] = r < G ? __ldg(qg + ks * 8 + 4) : 0u;
+            }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(qempty_bar(qslot));
-        if (++qslot == kQSlots) { qslot = 0; qphase ^= 1u; }
 
         float m0 = NEG_INF, m1 = NEG_INF, l0 = 0.f, l1 = 0.f;
         float o[8][4];
@@ -645,8 +700,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         // warp wait on a stage whose previous fill, owned by another warp, is
         // still in flight (TMA fills complete out of order); a parity wait
         // would then see the previous phase's parity and pass too early.
-        for (int jb = (warp - static_cast<int>(gidx0 % kConsumerWarps)) & (kConsumerWarps - 1); jb < len;
-             jb += kConsumerWarps) {
+        for (int jb = first; jb < len; jb += kConsumerWarps) {
             const int gi = gidx0 + jb;
             const int st = static_cast<int>(gi % kStages);
             mbar_wait(full_bar(st), static_cast<uint32_t>((gi / kStages) & 1), abort_flag, p.err);
@@ -718,27 +772,33 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         gidx0 += len;
 
         // ---- hand this warp's state for the piece to the merge warp ----
+        // (a warp without blocks in the piece writes nothing: the merge warp
+        // knows from the piece's geometry which warps contributed)
+        const int ms = piece % kMergeSlots;
+        if (mine) {
 #pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-            l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-            l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+            for (int off = 4; off < 32; off <<= 1) {
+                l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+                l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+            }
         }
-        const int ms = piece & 1;
-        mbar_wait(mempty_bar(ms), static_cast<uint32_t>(((piece >> 1) & 1) ^ 1), abort_flag, p.err);
-        float* o0 = sm_o + ms * kMergeOFloats + (warp * kMaxG + 2 * c) * kORow + r;
-        float* o1 = o0 + kORow;
+        mbar_wait(mempty_bar(ms), static_cast<uint32_t>(((piece / kMergeSlots) & 1) ^ 1), abort_flag, p.err);
+        if (mine) {
+            float* o0 = sm_o + ms * kMergeOFloats + (warp * kMaxG + 2 * c) * kORow + r;
+            float* o1 = o0 + kORow;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            o0[16 * j] = o[j][0];
-            o1[16 * j] = o[j][1];
-            o0[16 * j + 8] = o[j][2];
-            o1[16 * j + 8] = o[j][3];
-        }
-        if (r == 0) {
-            sm_m[ms * kMergeMLFloats + warp * kMaxG + 2 * c] = m0;
-            sm_m[ms * kMergeMLFloats + warp * kMaxG + 2 * c + 1] = m1;
-            sm_l[ms * kMergeMLFloats + warp * kMaxG + 2 * c] = l0;
-            sm_l[ms * kMergeMLFloats + warp * kMaxG + 2 * c + 1] = l1;
+            for (int j = 0; j < 8; ++j) {
+                o0[16 * j] = o[j][0];
+                o1[16 * j] = o[j][1];
+                o0[16 * j + 8] = o[j][2];
+                o1[16 * j + 8] = o[j][3];
+            }
+            if (r == 0) {
+                sm_m[ms * kMergeMLFloats + warp * kMaxG + 2 * c] = m0;
+                sm_m[ms * kMergeMLFloats + warp * kMaxG + 2 * c + 1] = m1;
+                sm_l[ms * kMergeMLFloats + warp * kMaxG + 2 * c] = l0;
+                sm_l[ms * kMergeMLFloats + warp * kMaxG + 2 * c + 1] = l1;
+            }
         }
         mbar_arrive(mfull_bar(ms));
         ++piece;
