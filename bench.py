@@ -62,6 +62,31 @@ def dist_info():
     return rank, world, local
 
 
+def max_over_ranks(value: float, world: int, device="cuda") -> float:
+    """The largest value over all ranks (the slowest rank's time); the value
+    itself for one rank."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_workload(name: str, rank: int, **kw):
+    """Weak scaling: every rank serves its own independent batch, seeded by
+    its rank (no data is exchanged between ranks)."""
+    from workloads import make_workload
+    return make_workload(name, seed=rank, **kw)
+
+
+def whole_job_rate(units_per_rank: int, world: int, ms: float) -> float:
+    """Units per second over all ranks: every rank processes its own units
+    in ms (the slowest rank's time)."""
+    return units_per_rank * world / (ms * 1e-3)
+
+
 def algorithmic_bytes(ctx, hq, hkv, d=128, block_tokens=16):
     """Decode attention's bytes per launch: every context token's K and V
     rows once, q and out, the table entries read and the lengths."""
@@ -70,6 +95,16 @@ def algorithmic_bytes(ctx, hq, hkv, d=128, block_tokens=16):
     qo = 2 * len(ctx) * hq * d * 2
     bt = int(((ctx + block_tokens - 1) // block_tokens).sum()) * 4
     return kv + qo + bt + len(ctx) * 4
+
+
+def unique_kv_bytes(tables, ctx, hkv, d=128, block_tokens=16):
+    """K and V bytes of the distinct physical blocks the launch reads: below
+    the algorithmic bytes when sequences share blocks (prefix groups, forks),
+    where the shared blocks can be served from L2 after their first read."""
+    used = set()
+    for row, c in zip(tables, np.asarray(ctx)):
+        used.update(int(b) for b in row[: (int(c) + block_tokens - 1) // block_tokens])
+    return len(used) * hkv * block_tokens * d * 2 * 2
 
 
 def measured_peak_gbs():
@@ -298,11 +333,9 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     import paged_kv_cache_49_gb300 as pkv
-    from workloads import make_workload
 
-    # Weak scaling: every rank serves its own independent batch (seed = rank).
     extra = {} if args.block_tokens == 16 else {"block_tokens": args.block_tokens}
-    w = make_workload(args.workload, seed=rank, **extra)
+    w = rank_workload(args.workload, rank, **extra)
     eng = pkv.PagedKVEngine(w.pool_blocks, w.num_q_heads, w.num_kv_heads, w.head_dim, free_order=w.free_order,
                             block_tokens=w.block_tokens)
     eng.load_workload_pool(w)
@@ -330,6 +363,11 @@ def run_ours(args):
                for _ in range(args.steps)]
     ev_attn = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(args.steps)]
+    # the step's cache kernels alone too (both idempotent for fixed inputs)
+    ev_app = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    ev_copy = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps if sb.num_pairs else 0)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -348,20 +386,32 @@ def run_ours(args):
             pkv.attn_decode(sb.q, eng.k_cache, eng.v_cache, sb.tables, sb.ctx, w.scale, sb.out,
                             sb.workspace, args.num_ctas)
             ev_attn[i][1].record(stream)
+        for i, (e0, e1) in enumerate(ev_app):
+            flush(i + 2)
+            e0.record(stream)
+            pkv.append(sb.k, sb.v, sb.slots, eng.k_cache, eng.v_cache, eng.error)
+            e1.record(stream)
+        for i, (e0, e1) in enumerate(ev_copy):
+            flush(i + 3)
+            e0.record(stream)
+            pkv.block_copy(eng.k_cache, eng.v_cache, sb.pairs, eng.error)
+            e1.record(stream)
         torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     step_ms = [a.elapsed_time(b) for a, b in ev_step]
     attn_ms = [a.elapsed_time(b) for a, b in ev_attn]
-    ms = statistics.mean(step_ms)
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = B * world / (ms * 1e-3)
+    ms = max_over_ranks(statistics.mean(step_ms), world)
+    value = whole_job_rate(B, world, ms)
     step_stats = {"min": min(step_ms), "median": statistics.median(step_ms), "max": max(step_ms)}
     attn_stats = {"min": min(attn_ms), "median": statistics.median(attn_ms), "max": max(attn_ms)}
-    launches = args.steps * (2 + (1 if sb.num_pairs else 0)) + args.steps
+
+    def stats_of(evs):
+        t = [a.elapsed_time(b) for a, b in evs]
+        return {"min": min(t), "median": statistics.median(t), "max": max(t)} if t else None
+
+    app_stats, copy_stats = stats_of(ev_app), stats_of(ev_copy)
+    launches = args.steps * (2 + (1 if sb.num_pairs else 0)) + args.steps + len(ev_app) + len(ev_copy)
     if eng.read_errors(sb):
         raise RuntimeError("device error word set during the timed steps")
 
@@ -386,24 +436,19 @@ def run_ours(args):
                 e1.synchronize()
                 if i >= args.warmup:
                     ts.append(e0.elapsed_time(e1))
-            t_ms = statistics.mean(ts)
-            if world > 1:
-                t = torch.tensor([t_ms], device="cuda")
-                dist.all_reduce(t, op=dist.ReduceOp.MAX)
-                t_ms = float(t.item())
-            return t_ms
+            return max_over_ranks(statistics.mean(ts), world)
 
         e2e_ms = timed(lambda: hs.run(w.scale, args.num_ctas))
         if not torch.equal(hs.out_host, sb.out.cpu()):
             raise RuntimeError("host-buffer step output differs from the device step")
-        e2e = {"value": B * world / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        e2e = {"value": whole_job_rate(B, world, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "call": "pkv_decode_step_host"}
         # The same call captured once in a CUDA graph and replayed (as a server does).
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
             hs.run(w.scale, args.num_ctas)
         g_ms = timed(graph.replay)
-        e2e["graph_replay"] = {"value": B * world / (g_ms * 1e-3), "ms_per_step": g_ms}
+        e2e["graph_replay"] = {"value": whole_job_rate(B, world, g_ms), "ms_per_step": g_ms}
 
     if rank != 0:
         if world > 1:
@@ -411,6 +456,7 @@ def run_ours(args):
         return
 
     abytes = algorithmic_bytes(ctx, w.num_q_heads, w.num_kv_heads, block_tokens=w.block_tokens)
+    ubytes = unique_kv_bytes(sb.tables.cpu().numpy(), ctx, w.num_kv_heads, block_tokens=w.block_tokens)
     attn_s = statistics.mean(attn_ms) * 1e-3
     peak, peak_kind = measured_peak_gbs()
     achieved = abytes / attn_s / 1e9
@@ -418,7 +464,8 @@ def run_ours(args):
                 "frac": achieved / peak, "traffic": recorded_traffic(w.name, int(ctx.sum())),
                 "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs copy bandwidth)",
                 "kernel": "pkv::attn::decode_kernel", "algorithmic_bytes_per_launch": abytes,
-                "attn_ms": attn_s * 1e3, "attn_ms_min": min(attn_ms), "frac_of_nominal_8tbs": achieved / 8000.0}
+                "attn_ms": attn_s * 1e3, "attn_ms_min": min(attn_ms), "frac_of_nominal_8tbs": achieved / 8000.0,
+                "unique_kv_bytes_per_launch": ubytes, "unique_kv_gbs": ubytes / attn_s / 1e9}
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         cpu = cpu_oracle_time(w)
@@ -432,7 +479,8 @@ def run_ours(args):
                    "num_ctas": args.num_ctas or pkv.default_ctas(B), "l2": "flushed before each timed launch (256 MiB write, then 256 MiB read: cold and clean)",
                    "parallelism": f"replicas x{world}"},
         "clocks": clk.summary(), "e2e": e2e, "gpu_launches": launches, "roofline": roofline,
-        "timing_ms": {"step": step_stats, "attention_alone": attn_stats},
+        "timing_ms": {"step": step_stats, "attention_alone": attn_stats, "append_alone": app_stats,
+                      "block_copy_alone": copy_stats},
         "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)
