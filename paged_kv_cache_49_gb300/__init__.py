@@ -7,10 +7,12 @@ engine that drives one attention layer's pool.
 """
 from ._native import (  # noqa: F401
     BLOCK_TOKENS, DEVERR_BLOCK_ID, DEVERR_CONTEXT, DEVERR_SLOT, DEVERR_TIMEOUT, EXPORTED,
-    HEAD_DIM, LIB_PATH, MAX_GROUP, AttentionWorkspace, BlockManager, PkvError, PoolExhausted,
+    HEAD_DIM, LIB_PATH, MAX_GROUP, AttentionWorkspace, BlockManager, Cascade, PkvError, PoolExhausted,
     ReservationExceeded, append, attn_decode, attn_decode_static, block_copy, decode_step, decode_step_host,
     default_ctas, new_error_word, step_layout,
     read_device_error,
 )
-from .engine import HostStep, PagedKVEngine, StepBuffers, bf16_from_bits, bits_from_bf16  # noqa: F401
+from .engine import (  # noqa: F401
+    HostStep, PagedKVEngine, StepBuffers, bf16_from_bits, bits_from_bf16, shared_prefix_groups,
+)
 from .graphs import GraphedDecoder, default_buckets  # noqa: F401

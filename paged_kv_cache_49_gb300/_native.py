@@ -41,6 +41,7 @@ EXPORTED = [
     "pkv_bm_refcount", "pkv_attn_decode_static", "pkv_decode_step", "pkv_attn_decode_ex", "pkv_append_ex",
     "pkv_block_copy_ex", "pkv_bm_create_ex", "pkv_bm_admit_tokens", "pkv_bm_preempt", "pkv_bm_resume",
     "pkv_bm_newest_running", "pkv_bm_slots", "pkv_step_layout", "pkv_decode_step_host",
+    "pkv_attn_cascade_workspace_size", "pkv_cascade_staging_size", "pkv_cascade_plan", "pkv_attn_decode_cascade",
 ]
 BLOCK_SIZES = (8, 16, 32, 64)
 
@@ -122,6 +123,11 @@ def _load() -> ctypes.CDLL:
         "pkv_bm_newest_running": (i32, [vp]),
         "pkv_bm_slots": (i32, [vp, i32, i32, i32, vp]),
         "pkv_step_layout": (i32, [i32, i32, i32, i32, i32, i32, vp]),
+        "pkv_attn_cascade_workspace_size": (sz, [i32, i32, i32, i32, vp, vp]),
+        "pkv_cascade_staging_size": (sz, [i32, i32, i32, i32, vp, vp]),
+        "pkv_cascade_plan": (i32, [i32, i32, i32, i32, vp, vp, vp, vp, sz, vp, sz, vp]),
+        "pkv_attn_decode_cascade": (i32, [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, f32, i32, vp, vp, vp, sz,
+                                          vp, vp]),
         "pkv_decode_step_host": (i32, [vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, i32, f32, i32, vp, sz, vp, vp,
                                        vp, vp]),
     }
@@ -350,6 +356,63 @@ def decode_step_host(host_packed, device_staging, num_pairs, k_cache, v_cache, m
                                      float(scale), int(num_ctas), workspace.ptr, workspace.nbytes,
                                      _ptr(device_out), _ptr(host_out), _ptr(device_error), _stream(stream)),
            "pkv_decode_step_host")
+
+
+class Cascade:
+    """Shared-prefix groups of a batch for pkv_attn_decode_cascade: each
+    group is (sequence indices of the batch, shared leading blocks). Owns the
+    device workspace and the pinned staging of the plan."""
+
+    def __init__(self, num_seqs: int, num_q_heads: int, num_kv_heads: int, groups, device=None, stream=None):
+        groups = [(list(map(int, m)), int(sh)) for m, sh in groups]
+        self.num_seqs, self.num_q_heads, self.num_kv_heads = num_seqs, num_q_heads, num_kv_heads
+        self.groups = groups
+        offs = [0]
+        for m, _ in groups:
+            offs.append(offs[-1] + len(m))
+        n = len(groups)
+        self._offsets = (ctypes.c_int32 * (n + 1))(*offs)
+        self._members = (ctypes.c_int32 * max(1, offs[-1]))(*[x for m, _ in groups for x in m])
+        self._shared = (ctypes.c_int32 * max(1, n))(*[sh for _, sh in groups])
+        args = (num_seqs, num_q_heads, num_kv_heads, n, self._offsets, self._shared)
+        self.nbytes = int(_lib.pkv_attn_cascade_workspace_size(*args))
+        staging = int(_lib.pkv_cascade_staging_size(*args))
+        if self.nbytes == 0 or staging == 0:
+            raise PkvError(PKV_EINVAL, "pkv_attn_cascade_workspace_size")
+        self.buffer = torch.empty(self.nbytes + 256, dtype=torch.uint8, device=device or "cuda")
+        off = (-self.buffer.data_ptr()) % 256
+        self.tensor = self.buffer[off: off + self.nbytes]
+        self.staging = torch.empty(staging, dtype=torch.uint8).pin_memory()
+        _check(_lib.pkv_attn_workspace_init(self.tensor.data_ptr(), self.nbytes, _stream(stream)),
+               "pkv_attn_workspace_init")
+        _check(_lib.pkv_cascade_plan(num_seqs, num_q_heads, num_kv_heads, n, self._offsets, self._members, self._shared,
+                                     self.tensor.data_ptr(), self.nbytes, self.staging.data_ptr(), staging,
+                                     _stream(stream)), "pkv_cascade_plan")
+
+    def decode(self, q, k_cache, v_cache, block_tables, context_lens, scale, out=None, stream=None):
+        """Decode attention for the batch the groups describe; returns out."""
+        _need(q, torch.bfloat16, "q")
+        _need(k_cache, torch.bfloat16, "k_cache")
+        _need(v_cache, torch.bfloat16, "v_cache")
+        _need(block_tables, torch.int32, "block_tables")
+        _need(context_lens, torch.int32, "context_lens")
+        B, hq, d = q.shape
+        nb, hkv, bt, _ = k_cache.shape
+        if (B, hq, hkv) != (self.num_seqs, self.num_q_heads, self.num_kv_heads) or bt != BLOCK_TOKENS:
+            raise ValueError("batch shape differs from the plan's, or blocks are not 16 tokens")
+        if out is None:
+            out = torch.empty_like(q)
+        _need(out, torch.bfloat16, "out")
+        _check(_lib.pkv_attn_decode_cascade(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                            block_tables.shape[1], _ptr(context_lens), B, hq, hkv, d, nb,
+                                            float(scale), len(self.groups), self._offsets, self._shared,
+                                            self.tensor.data_ptr(), self.nbytes, _ptr(out), _stream(stream)),
+               "pkv_attn_decode_cascade")
+        return out
+
+    def read_error(self, clear: bool = True, stream=None) -> int:
+        """The device error word the three kernels share (then cleared)."""
+        return read_device_error(self.tensor[:4].view(torch.int32), clear, stream)
 
 
 def attn_decode_static(q, k_cache, v_cache, block_tables, context_lens, scale, out, device_error=None,

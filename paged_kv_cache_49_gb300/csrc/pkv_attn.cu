@@ -44,7 +44,9 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
+#include <cstring>
 #include <map>
 #include <mutex>
 #include <utility>
@@ -89,8 +91,14 @@ constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kOffScan = kOffMisc + 64;
 
 // Dynamic shared memory: the fixed part, the prefix sum (4 bytes per
-// sequence) and each sequence's last-tile token count (1 byte per sequence).
-constexpr size_t smem_bytes(int num_seqs) { return 1024 + kOffScan + 5 * static_cast<size_t>(num_seqs); }
+// sequence), each sequence's last-tile token count (1 byte per sequence) and,
+// when leading tiles are skipped (the private pass of cascade attention), each
+// sequence's skipped tile count (4 bytes per sequence).
+__host__ __device__ constexpr size_t skip_offset(int num_seqs) { return (kOffScan + 5 * static_cast<size_t>(num_seqs) + 3) & ~size_t(3); }
+constexpr size_t smem_bytes(int num_seqs, bool skip = false) {
+    return 1024 + (skip ? skip_offset(num_seqs) + 4 * static_cast<size_t>(num_seqs)
+                        : kOffScan + 5 * static_cast<size_t>(num_seqs));
+}
 
 constexpr size_t kWsHeader = 256;
 
@@ -117,6 +125,12 @@ struct Params {
     uint32_t* err;
     int* counters;
     float* partials;
+    // Cascade attention's private pass (both null otherwise): per sequence,
+    // leading tiles to skip (computed elsewhere), and where a sequence with
+    // skipped tiles leaves its unnormalised fp32 result instead of an output
+    // row ([num_seqs * num_q_heads][kORow]: output, max, sum).
+    const int32_t* skip_tiles;
+    float* side;
 };
 
 // Position in the line of (sequence, KV head) block runs.
@@ -235,6 +249,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
 
     int* scan = reinterpret_cast<int*>(smem + kOffScan);
     uint8_t* tail = smem + kOffScan + 4 * static_cast<size_t>(B);  // tokens in each sequence's last tile
+    int* skip = p.skip_tiles ? reinterpret_cast<int*>(smem + skip_offset(B)) : nullptr;
+    auto skipped = [&](int s) { return skip ? skip[s] : 0; };
     int* misc = reinterpret_cast<int*>(smem + kOffMisc);
     volatile int* abort_flag = misc;  // misc[0]
     int* warp_tot = misc + 8;         // misc[8 .. 8 + kThreads / 32)
@@ -281,7 +297,17 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             const int c = __ldg(p.context_lens + s);
             if (c > cap && p.err) atomicOr(p.err, PKV_DEVERR_CONTEXT);
             const int cc = min(c, cap);
-            local += cc > 0 ? (cc + kTok - 1) / kTok : 0;
+            const int all = cc > 0 ? (cc + kTok - 1) / kTok : 0;
+            int sk = 0;
+            if (skip) {
+                sk = __ldg(p.skip_tiles + s);
+                if (sk < 0 || sk > all) {  // more skipped tiles than the context holds
+                    if (p.err) atomicOr(p.err, PKV_DEVERR_CONTEXT);
+                    sk = sk < 0 ? 0 : all;
+                }
+                skip[s] = sk;
+            }
+            local += all - sk;
         }
         int v = local;
 #pragma unroll
@@ -296,7 +322,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         for (int s = lo; s < hi; ++s) {
             const int cc = clamped_ctx(p, s);
             const int tiles = cc > 0 ? (cc + kTok - 1) / kTok : 0;
-            run += tiles;
+            run += tiles - (skip ? skip[s] : 0);
             scan[s] = run;
             tail[s] = static_cast<uint8_t>(cc - kTok * (tiles - 1));  // 1..16 (unused when tiles == 0)
         }
@@ -323,9 +349,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             for (const char* x = line + lane * 128; x < hi; x += 32 * 128) prefetch_l2(x);
         };
         warm(reinterpret_cast<const char*>(p.block_tables + static_cast<size_t>(a.s) * p.max_blocks +
-                                           a.blk * kTok / kBT),
+                                           (skipped(a.s) + a.blk) * kTok / kBT),
              reinterpret_cast<const char*>(p.block_tables + static_cast<size_t>(z.s) * p.max_blocks +
-                                           ((z.blk + 1) * kTok + kBT - 1) / kBT));
+                                           ((skipped(z.s) + z.blk + 1) * kTok + kBT - 1) / kBT));
         warm(reinterpret_cast<const char*>(p.q + (static_cast<size_t>(a.s) * p.num_q_heads +
                                                   static_cast<size_t>(a.g) * G) * kDim),
              reinterpret_cast<const char*>(p.q + (static_cast<size_t>(z.s) * p.num_q_heads +
@@ -381,7 +407,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 if (++qslot == kQSlots) { qslot = 0; qphase ^= 1u; }
             }
             const int32_t* row = p.block_tables + static_cast<size_t>(pc.s) * p.max_blocks;
-            const int seq_blocks = (kTok * (pc.nb - 1) + tail[pc.s] + kBT - 1) / kBT;  // valid table entries
+            const int sk0 = skipped(pc.s);  // the run starts at the sequence's tile sk0
+            const int seq_blocks = (kTok * (sk0 + pc.nb - 1) + tail[pc.s] + kBT - 1) / kBT;  // valid table entries
             auto block_id = [&](int e) {
                 int bid = __ldg(row + e);
                 if (bid < 0 || bid >= p.num_blocks) {
@@ -393,7 +420,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             for (int j0 = 0; j0 < len; j0 += 32) {
                 int y0 = 0, y1 = 0;  // token-row coordinates of the tile's rows 0 and 8
                 if (j0 + lane < len) {
-                    const int t = pc.blk + j0 + lane;  // tile index within the sequence
+                    const int t = sk0 + pc.blk + j0 + lane;  // tile index within the sequence
                     if constexpr (kBT >= kTok) {
                         y0 = (block_id(t / (kBT / kTok)) * Hkv + pc.g) * kBT + (t % (kBT / kTok)) * kTok;
                     } else {
@@ -484,6 +511,28 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             __nv_bfloat16* out_base =
                 p.out + (static_cast<size_t>(s) * p.num_q_heads + static_cast<size_t>(g) * G) * kDim + d0;
             float* part = p.partials + (static_cast<size_t>(blockIdx.x) * 2 + (pc.start == range_lo ? 0 : 1)) * kPartialFloats;
+            // The pair's finished result for head h: a bf16 output row, or, for
+            // a sequence whose leading tiles another pass covers, its
+            // unnormalised fp32 result for the cascade merge.
+            const bool to_side = p.side && skipped(s) > 0;
+            float* side_base = to_side ? p.side + (static_cast<size_t>(s) * p.num_q_heads + static_cast<size_t>(g) * G) * kORow
+                                       : nullptr;
+            auto emit = [&](int h, float4 acc, float M, float L) {
+                if (to_side) {
+                    float* sd = side_base + static_cast<size_t>(h) * kORow;
+                    *reinterpret_cast<float4*>(sd + d0) = acc;
+                    if (lane == 0) {
+                        sd[kDim] = M;
+                        sd[kDim + 1] = L;
+                    }
+                } else {
+                    const float inv = 1.f / L;
+                    uint2 w2;
+                    w2.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+                    w2.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+                    *reinterpret_cast<uint2*>(out_base + static_cast<size_t>(h) * kDim) = w2;
+                }
+            };
             // Four heads at a time: every shared-memory read of the four
             // heads' warp states is issued before any of them is used.
 #pragma unroll
@@ -527,11 +576,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                                 acc.w += f * ok[w][hh].w;
                             }
                             if (pieces == 1) {
-                                const float inv = 1.f / L;
-                                uint2 w2;
-                                w2.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-                                w2.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-                                *reinterpret_cast<uint2*>(out_base + static_cast<size_t>(h) * kDim) = w2;
+                                emit(h, acc, M, L);
                             } else {
                                 *reinterpret_cast<float4*>(part + h * kORow + d0) = acc;
                                 if (lane == 0) {
@@ -619,15 +664,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                         }
                     }
 #pragma unroll
-                    for (int h = 0; h < kMaxG; ++h) {
-                        if (h < G) {
-                            const float inv = 1.f / Lr[h];
-                            uint2 w2;
-                            w2.x = pack_bf16x2(Ar[h].x * inv, Ar[h].y * inv);
-                            w2.y = pack_bf16x2(Ar[h].z * inv, Ar[h].w * inv);
-                            *reinterpret_cast<uint2*>(out_base + static_cast<size_t>(h) * kDim) = w2;
-                        }
-                    }
+                    for (int h = 0; h < kMaxG; ++h)
+                        if (h < G) emit(h, Ar[h], Mr[h], Lr[h]);
                     if (lane == 0) p.counters[s * Hkv + g] = 0;  // ready for the next launch
                 }
             }
@@ -871,7 +909,7 @@ DeviceInfo device_info() {
     for (int bt : {8, 16, 32, 64})
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(kernel_for(bt), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(smem_bytes(PKV_ATTN_MAX_SEQS)));
+                                     static_cast<int>(smem_bytes(PKV_ATTN_MAX_SEQS, true)));
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) {
         record_cuda_error(e);
@@ -884,7 +922,7 @@ DeviceInfo device_info() {
 // Persistent CTAs for a batch of num_seqs: every CTA that fits at once (the
 // shared-memory prefix sum grows with num_seqs, so large batches may fit one
 // CTA per SM instead of two). 0 on error.
-int grid_for(int num_seqs, int block_tokens = PKV_BLOCK_TOKENS) {
+int grid_for(int num_seqs, int block_tokens = PKV_BLOCK_TOKENS, bool skip = false) {
     const DeviceInfo d = device_info();
     const KernelFn fn = kernel_for(block_tokens);
     if (!d.ok || !fn) return 0;
@@ -894,7 +932,7 @@ int grid_for(int num_seqs, int block_tokens = PKV_BLOCK_TOKENS) {
     static std::map<std::pair<int, size_t>, int> cache;
     int dev = 0;
     cudaGetDevice(&dev);
-    const size_t smem = smem_bytes(num_seqs);
+    const size_t smem = smem_bytes(num_seqs, skip);
     const std::pair<int, size_t> key{dev * 128 + block_tokens, smem};
     {
         std::lock_guard<std::mutex> lock(mu);
@@ -973,6 +1011,8 @@ pkv_status prepare(const void* q, const void* k_cache, const void* v_cache, cons
     prm.err = reinterpret_cast<uint32_t*>(ws);
     prm.counters = reinterpret_cast<int*>(ws + kWsHeader);
     prm.partials = reinterpret_cast<float*>(ws + fixed);
+    prm.skip_tiles = nullptr;
+    prm.side = nullptr;
     L->grid = grid;
     L->smem = smem_bytes(num_seqs);
     return PKV_OK;
@@ -1197,6 +1237,603 @@ pkv_status pkv_decode_step_host(const void* host_packed, void* device_staging, i
 }  // extern "C"
 
 // ---------------------------------------------------------------------------
+// Cascade attention: shared prefix blocks read once for all their sharers.
+//
+// Sequences that share their leading blocks (a prompt forked into parallel
+// samples, requests of one prefix group) would otherwise each stream the same
+// prefix from HBM ("KV cache systems" and cs2680 Lecture 10, §10.4: the shared
+// blocks are one copy in memory; here they are also one read). A decode step
+// over such a batch runs three kernels:
+//  1. prefix_kernel: for every group, KV head and 32-row chunk of the group's
+//     query rows (sharers x heads of the GQA group), one pass over at most 64
+//     shared tiles, all four consumer warps reading every tile for 8 rows
+//     each; each pass leaves fp32 partials (output, max, sum) per row.
+//  2. decode_kernel with skip_tiles: the private rest of every sequence; a
+//     sequence with skipped tiles leaves its fp32 result in `side`.
+//  3. cascade_merge_kernel: per grouped (sequence, KV head), the log-sum-exp
+//     merge of its prefix partials and its private result, in a fixed order.
+// The pages speak of sharing the memory only; sharing the reads is this
+// library's own step, and it changes only the order of the sums.
+
+namespace pkv {
+namespace attn {
+
+constexpr int kPfxRows = 32;     // query rows per prefix item: 8 per consumer warp
+constexpr int kPfxTiles = 64;    // shared tiles per prefix item at most
+constexpr int kPfxThreads = kConsumers + 32;
+constexpr int kPfxOffBar = kStages * kStageBytes;
+constexpr size_t kPfxSmem = 1024 + kPfxOffBar + 2 * kStages * 8 + 64;
+
+struct PrefixParams {
+    const __nv_bfloat16* q;
+    const int32_t* block_tables;
+    int max_blocks;
+    int num_q_heads;
+    int num_kv_heads;
+    int group;
+    int num_blocks;
+    float scale_log2;
+    const int32_t* members;  // sequence ids of each group's sharers, group after group
+    const int4* items;       // x: first sharer (index into members), y: valid rows,
+                             // z: KV head | tiles << 16, w: first shared tile
+    int num_items;
+    uint32_t* err;
+    float* wpart;            // [num_items][kPfxRows][kORow]
+};
+
+__global__ void __launch_bounds__(kPfxThreads, 1)
+prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+              const PrefixParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int G = p.group;
+    const int Hkv = p.num_kv_heads;
+    const uint32_t bar0 = smem_u32(smem + kPfxOffBar);
+    auto full_bar = [&](int i) { return bar0 + 8u * i; };
+    auto empty_bar = [&](int i) { return bar0 + 8u * (kStages + i); };
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kPfxOffBar + 2 * kStages * 8);
+    if (warp == kProducerWarp && lane == 0) {
+        prefetch_tensormap(&tm_k);
+        prefetch_tensormap(&tm_v);
+    }
+    if (tid == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(full_bar(i), 1);
+            mbar_init(empty_bar(i), kConsumerWarps);  // every consumer warp reads every stage
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == kProducerWarp) {
+        const uint64_t policy = policy_evict_first();
+        int stage = 0, issued = 0;
+        uint32_t sphase = 0;
+        for (int it = blockIdx.x; it < p.num_items; it += gridDim.x) {
+            const int4 item = p.items[it];
+            const int g = item.z & 0xffff, n = item.z >> 16;
+            const int32_t* row = p.block_tables + static_cast<size_t>(__ldg(p.members + item.x)) * p.max_blocks;
+            for (int j0 = 0; j0 < n; j0 += 32) {
+                int y0 = 0;
+                if (j0 + lane < n) {
+                    int bid = __ldg(row + item.w + j0 + lane);
+                    if (bid < 0 || bid >= p.num_blocks) {
+                        if (p.err) atomicOr(p.err, PKV_DEVERR_BLOCK_ID);
+                        bid = 0;
+                    }
+                    y0 = (bid * Hkv + g) * kTok;
+                }
+                const int cnt = min(32, n - j0);
+                for (int jj = 0; jj < cnt; ++jj) {
+                    const int ya = __shfl_sync(0xffffffffu, y0, jj);
+                    if (lane == 0 && mbar_wait(empty_bar(stage), sphase ^ 1u, abort_flag, p.err)) {
+                        const uint32_t fb = full_bar(stage);
+                        mbar_arrive_expect_tx(fb, kStageBytes);
+                        const uint32_t dst = smem_u32(smem + stage * kStageBytes);
+                        tma_load_2d(dst, &tm_k, 0, ya, fb, policy);
+                        tma_load_2d(dst + kHalfBytes, &tm_k, 64, ya, fb, policy);
+                        tma_load_2d(dst + kBlockBytes, &tm_v, 0, ya, fb, policy);
+                        tma_load_2d(dst + kBlockBytes + kHalfBytes, &tm_v, 64, ya, fb, policy);
+                        ++issued;
+                    }
+                    if (++stage == kStages) { stage = 0; sphase ^= 1u; }
+                }
+            }
+        }
+        if (lane == 0) {  // no copy may land after the CTA exits (bounded waits)
+            volatile int never = 0;
+            for (int i = max(0, issued - kStages); i < issued; ++i)
+                mbar_wait(full_bar(i % kStages), static_cast<uint32_t>((i / kStages) & 1), &never, nullptr);
+        }
+        return;
+    }
+
+    // consumer warps: rows 8 * warp + (0..7) of each item
+    const int r = lane >> 2;
+    const int c = lane & 3;
+    const uint32_t k_row_off = static_cast<uint32_t>(lane & 15) * 128u;
+    const int k_sw = lane & 7;
+    const int k_hi = lane >> 4;
+    const int v_mat = lane >> 3;
+    const uint32_t v_row_off = static_cast<uint32_t>((lane & 7) + ((v_mat >> 1) << 3)) * 128u;
+    const int v_sw = lane & 7;
+    const float NEG_INF = -INFINITY;
+    int gi = 0;  // the CTA's tile count so far: stage gi % kStages
+    for (int it = blockIdx.x; it < p.num_items; it += gridDim.x) {
+        const int4 item = p.items[it];
+        const int g = item.z & 0xffff, n = item.z >> 16;
+        const int row = 8 * warp + r;  // this lane's query row (mma column) in the item
+        const bool valid_row = row < item.y;
+        uint32_t qb[16];
+        {
+            const int seq = valid_row ? __ldg(p.members + item.x + row / G) : 0;
+            const uint32_t* qg = reinterpret_cast<const uint32_t*>(
+                p.q + (static_cast<size_t>(seq) * p.num_q_heads + static_cast<size_t>(g) * G + row % G) * kDim) + c;
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                qb[2 * ks] = valid_row ? __ldg(qg + ks * 8) : 0u;
+                qb[2 * ks + 1] = valid_row ? __ldg(qg + ks * 8 + 4) : 0u;
+            }
+        }
+        float m0 = NEG_INF, m1 = NEG_INF, l0 = 0.f, l1 = 0.f;
+        float o[8][4];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+        for (int t = 0; t < n; ++t, ++gi) {
+            const int st = gi % kStages;
+            mbar_wait(full_bar(st), static_cast<uint32_t>((gi / kStages) & 1), abort_flag, p.err);
+            const uint32_t sk = smem_u32(smem + st * kStageBytes);
+            const uint32_t sv = sk + kBlockBytes;
+            float sa[4] = {0.f, 0.f, 0.f, 0.f};
+            float sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const int chunk = ((ks & 3) << 1) | k_hi;
+                uint32_t a[4];
+                ldmatrix_x4(a, sk + (ks >> 2) * kHalfBytes + k_row_off + ((chunk ^ k_sw) << 4));
+                if (ks & 1) mma_bf16_16816(sb, a, qb[2 * ks], qb[2 * ks + 1]);
+                else mma_bf16_16816(sa, a, qb[2 * ks], qb[2 * ks + 1]);
+            }
+            // shared tiles are whole blocks: all 16 tokens are valid
+            const float x0 = (sa[0] + sb[0]) * p.scale_log2, x1 = (sa[1] + sb[1]) * p.scale_log2;
+            const float x2 = (sa[2] + sb[2]) * p.scale_log2, x3 = (sa[3] + sb[3]) * p.scale_log2;
+            float bm0 = fmaxf(x0, x2), bm1 = fmaxf(x1, x3);
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
+                bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
+            }
+            const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
+            const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);
+            m0 = mn0;
+            m1 = mn1;
+            const uint32_t p01 = pack_bf16x2(ex2(x0 - mn0), ex2(x1 - mn1));
+            const uint32_t p23 = pack_bf16x2(ex2(x2 - mn0), ex2(x3 - mn1));
+            l0 = l0 * al0 + bf16_lo(p01) + bf16_lo(p23);
+            l1 = l1 * al1 + bf16_hi(p01) + bf16_hi(p23);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                o[j][0] *= al0;
+                o[j][1] *= al1;
+                o[j][2] *= al0;
+                o[j][3] *= al1;
+            }
+            const uint32_t pb0 = movmatrix_trans(p01);
+            const uint32_t pb1 = movmatrix_trans(p23);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int chunk = ((j & 3) << 1) | (v_mat & 1);
+                uint32_t a[4];
+                ldmatrix_x4_trans(a, sv + (j >> 2) * kHalfBytes + v_row_off + ((chunk ^ v_sw) << 4));
+                mma_bf16_16816(o[j], a, pb0, pb1);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty_bar(st));
+        }
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+        }
+        // rows 8w + 2c and 8w + 2c + 1: dims 16j + r (o[j][0..1]) and 16j + r + 8 (o[j][2..3])
+        float* w0 = p.wpart + (static_cast<size_t>(it) * kPfxRows + 8 * warp + 2 * c) * kORow;
+        float* w1 = w0 + kORow;
+        if (8 * warp + 2 * c < item.y) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                w0[16 * j + r] = o[j][0];
+                w0[16 * j + r + 8] = o[j][2];
+            }
+            if (r == 0) {
+                w0[kDim] = m0;
+                w0[kDim + 1] = l0;
+            }
+        }
+        if (8 * warp + 2 * c + 1 < item.y) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                w1[16 * j + r] = o[j][1];
+                w1[16 * j + r + 8] = o[j][3];
+            }
+            if (r == 0) {
+                w1[kDim] = m1;
+                w1[kDim + 1] = l1;
+            }
+        }
+    }
+}
+
+struct MergeParams {
+    const float* wpart;
+    const float* side;
+    __nv_bfloat16* out;
+    const int4* targets;  // x: sequence, y: KV head | shared tiles << 16,
+                          // z: first prefix item, w: prefix items | first row << 16
+    const int32_t* context_lens;
+    int cap_tokens;
+    int num_targets;
+    int num_q_heads;
+    int group;
+};
+
+// One warp per grouped (sequence, KV head): lane l owns dims [4l, 4l + 4) of
+// every head; the partials are merged in a fixed order (prefix items, then
+// the private result), four partials and four heads per batch of loads.
+__global__ void __launch_bounds__(128) cascade_merge_kernel(const MergeParams p) {
+    const int warp_id = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (warp_id >= p.num_targets) return;
+    const int4 tg = p.targets[warp_id];
+    const int s = tg.x, g = tg.y & 0xffff;
+    const int ctx = min(__ldg(p.context_lens + s), p.cap_tokens);
+    const bool has_private = (ctx + kTok - 1) / kTok > (tg.y >> 16);  // the private pass left a result
+    const int n_items = tg.w & 0xffff, row0 = tg.w >> 16;
+    const int G = p.group;
+    const int np = n_items + (has_private ? 1 : 0);
+    const int d0 = lane * 4;
+    const float NEG_INF = -INFINITY;
+    auto part_ptr = [&](int k, int h) -> const float* {
+        if (k < n_items) return p.wpart + (static_cast<size_t>(tg.z + k) * kPfxRows + row0 + h) * kORow;
+        return p.side + ((static_cast<size_t>(s) * p.num_q_heads + static_cast<size_t>(g) * G + h) * kORow);
+    };
+    float Mr[kMaxG], Lr[kMaxG];
+    float4 Ar[kMaxG];
+#pragma unroll
+    for (int h = 0; h < kMaxG; ++h) {
+        Mr[h] = NEG_INF;
+        Lr[h] = 0.f;
+        Ar[h] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    for (int i = 0; i < np; i += 4) {
+#pragma unroll
+        for (int hb = 0; hb < kMaxG; hb += 4) {
+            if (hb < G) {
+                float mk[4][4], lk[4][4];
+                float4 ok[4][4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        if (i + k < np && hb + h < G) {
+                            const float* pp = part_ptr(i + k, hb + h);
+                            mk[k][h] = __ldcg(pp + kDim);
+                            lk[k][h] = __ldcg(pp + kDim + 1);
+                            ok[k][h] = __ldcg(reinterpret_cast<const float4*>(pp + d0));
+                        } else {
+                            mk[k][h] = NEG_INF;
+                            lk[k][h] = 0.f;
+                            ok[k][h] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    const int H = hb + h;
+                    if (H < G) {
+                        float mn = Mr[H];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) mn = fmaxf(mn, mk[k][h]);
+                        const float a = ex2(Mr[H] - mn);
+                        float L = Lr[H] * a;
+                        float4 A = make_float4(Ar[H].x * a, Ar[H].y * a, Ar[H].z * a, Ar[H].w * a);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const float b = ex2(mk[k][h] - mn);
+                            L += b * lk[k][h];
+                            A.x += b * ok[k][h].x;
+                            A.y += b * ok[k][h].y;
+                            A.z += b * ok[k][h].z;
+                            A.w += b * ok[k][h].w;
+                        }
+                        Mr[H] = mn;
+                        Lr[H] = L;
+                        Ar[H] = A;
+                    }
+                }
+            }
+        }
+    }
+    __nv_bfloat16* out_base = p.out + (static_cast<size_t>(s) * p.num_q_heads + static_cast<size_t>(g) * G) * kDim + d0;
+#pragma unroll
+    for (int h = 0; h < kMaxG; ++h) {
+        if (h < G) {
+            const float inv = 1.f / Lr[h];
+            uint2 w2;
+            w2.x = pack_bf16x2(Ar[h].x * inv, Ar[h].y * inv);
+            w2.y = pack_bf16x2(Ar[h].z * inv, Ar[h].w * inv);
+            *reinterpret_cast<uint2*>(out_base + static_cast<size_t>(h) * kDim) = w2;
+        }
+    }
+}
+
+// Host-side layout of a cascade plan inside the caller's workspace.
+struct CascadeLayout {
+    size_t decode_bytes, side_off, skip_off, members_off, items_off, targets_off, wpart_off, total;
+    int num_items, num_targets, total_members;
+    int chunk_tiles;  // shared tiles per prefix item (8..kPfxTiles)
+};
+
+pkv_status cascade_layout(int num_seqs, int num_q_heads, int num_kv_heads, int num_groups,
+                          const int32_t* group_offsets, const int32_t* group_shared_blocks, CascadeLayout* L) {
+    if (num_seqs < 1 || num_seqs > PKV_ATTN_MAX_SEQS || num_kv_heads < 1 || num_q_heads < 1 ||
+        num_q_heads % num_kv_heads != 0 || num_q_heads / num_kv_heads > PKV_ATTN_MAX_GROUP || num_groups < 0 ||
+        (num_groups > 0 && (!group_offsets || !group_shared_blocks)))
+        return PKV_EINVAL;
+    const int G = num_q_heads / num_kv_heads;
+    long long items = 0, targets = 0, passes = 0;
+    if (num_groups > 0 && group_offsets[0] != 0) return PKV_EINVAL;
+    for (int gr = 0; gr < num_groups; ++gr) {
+        const int m = group_offsets[gr + 1] - group_offsets[gr];
+        const int sh = group_shared_blocks[gr];
+        if (m < 1 || sh < 1) return PKV_EINVAL;
+        if (sh > 0xffff) return PKV_ERANGE;
+        passes += static_cast<long long>(num_kv_heads) * ((static_cast<long long>(m) * G + kPfxRows - 1) / kPfxRows) * sh;
+        targets += static_cast<long long>(m) * num_kv_heads;
+    }
+    // Cut shared prefixes so that the prefix pass has about two items per
+    // CTA slot: small batches get short items (more parallel reads), large
+    // ones long items (fewer partials to merge).
+    const DeviceInfo dev = device_info();
+    if (!dev.ok) return PKV_ECUDA;
+    const long long slots = 3ll * dev.sm_count;
+    int chunk = static_cast<int>(std::min<long long>(kPfxTiles, std::max<long long>(8, (passes + 2 * slots - 1) / (2 * slots))));
+    L->chunk_tiles = chunk;
+    for (int gr = 0; gr < num_groups; ++gr) {
+        const int m = group_offsets[gr + 1] - group_offsets[gr];
+        const long long chunks = (static_cast<long long>(m) * G + kPfxRows - 1) / kPfxRows;
+        items += num_kv_heads * chunks * ((group_shared_blocks[gr] + chunk - 1) / chunk);
+    }
+    const int total_members = num_groups > 0 ? group_offsets[num_groups] : 0;
+    if (total_members > num_seqs || items > (1 << 28)) return PKV_ERANGE;
+    const int grid = grid_for(num_seqs);
+    if (grid < 1) return PKV_ECUDA;
+    L->decode_bytes = align256(workspace_bytes(num_seqs, num_kv_heads, grid));
+    L->side_off = L->decode_bytes;
+    L->skip_off = L->side_off + align256(static_cast<size_t>(num_seqs) * num_q_heads * kORow * 4);
+    L->members_off = L->skip_off + align256(static_cast<size_t>(num_seqs) * 4);
+    L->items_off = L->members_off + align256(static_cast<size_t>(total_members) * 4 + 4);
+    L->targets_off = L->items_off + align256(static_cast<size_t>(items) * 16 + 16);
+    L->wpart_off = L->targets_off + align256(static_cast<size_t>(targets) * 16 + 16);
+    L->total = L->wpart_off + static_cast<size_t>(items) * kPfxRows * kORow * 4;
+    L->num_items = static_cast<int>(items);
+    L->num_targets = static_cast<int>(targets);
+    L->total_members = total_members;
+    return PKV_OK;
+}
+
+// Per device, once: the side stream the prefix pass runs on, concurrently
+// with the private pass, and the two events that fork it from and join it to
+// the caller's stream.
+struct SideStream {
+    cudaStream_t stream = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+bool side_stream(SideStream* out) {
+    static std::mutex mu;
+    static std::vector<SideStream> per_dev;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        record_cuda_error(e);
+        return false;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (static_cast<int>(per_dev.size()) <= dev) per_dev.resize(dev + 1);
+    SideStream& ss = per_dev[dev];
+    if (!ss.stream) {
+        e = cudaStreamCreateWithFlags(&ss.stream, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming);
+        if (e != cudaSuccess) {
+            record_cuda_error(e);
+            ss = SideStream{};
+            return false;
+        }
+    }
+    *out = ss;
+    return true;
+}
+
+}  // namespace attn
+}  // namespace pkv
+
+extern "C" {
+
+size_t pkv_attn_cascade_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int num_groups,
+                                       const int32_t* group_offsets, const int32_t* group_shared_blocks) {
+    attn::CascadeLayout L;
+    if (attn::cascade_layout(num_seqs, num_q_heads, num_kv_heads, num_groups, group_offsets, group_shared_blocks,
+                             &L) != PKV_OK)
+        return 0;
+    return L.total;
+}
+
+size_t pkv_cascade_staging_size(int num_seqs, int num_q_heads, int num_kv_heads, int num_groups,
+                                const int32_t* group_offsets, const int32_t* group_shared_blocks) {
+    attn::CascadeLayout L;
+    if (attn::cascade_layout(num_seqs, num_q_heads, num_kv_heads, num_groups, group_offsets, group_shared_blocks,
+                             &L) != PKV_OK)
+        return 0;
+    return L.wpart_off - L.skip_off;
+}
+
+pkv_status pkv_cascade_plan(int num_seqs, int num_q_heads, int num_kv_heads, int num_groups,
+                            const int32_t* group_offsets, const int32_t* group_members,
+                            const int32_t* group_shared_blocks, void* workspace, size_t workspace_bytes,
+                            void* host_staging, size_t staging_bytes, void* stream) {
+    attn::CascadeLayout L;
+    pkv_status st = attn::cascade_layout(num_seqs, num_q_heads, num_kv_heads, num_groups, group_offsets,
+                                         group_shared_blocks, &L);
+    if (st != PKV_OK) return st;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < L.total) return PKV_EINVAL;
+    if (!host_staging || (num_groups > 0 && !group_members)) return PKV_EINVAL;
+    const size_t upload = L.wpart_off - L.skip_off;
+    if (staging_bytes < upload) return PKV_EINVAL;
+    const int G = num_q_heads / num_kv_heads;
+    uint8_t* h = static_cast<uint8_t*>(host_staging);
+    std::memset(h, 0, upload);
+    int32_t* skip = reinterpret_cast<int32_t*>(h);
+    int32_t* members = reinterpret_cast<int32_t*>(h + (L.members_off - L.skip_off));
+    int4* items = reinterpret_cast<int4*>(h + (L.items_off - L.skip_off));
+    int4* targets = reinterpret_cast<int4*>(h + (L.targets_off - L.skip_off));
+    std::vector<char> seen(num_seqs, 0);
+    int ni = 0, nt = 0;
+    for (int gr = 0; gr < num_groups; ++gr) {
+        const int b = group_offsets[gr], e = group_offsets[gr + 1];
+        const int sh = group_shared_blocks[gr];
+        const int m = e - b;
+        for (int k = b; k < e; ++k) {
+            const int sq = group_members[k];
+            if (sq < 0 || sq >= num_seqs || seen[sq]) return PKV_EINVAL;  // one group per sequence
+            seen[sq] = 1;
+            members[k] = sq;
+            skip[sq] = sh;
+        }
+        const int chunks = (m * G + attn::kPfxRows - 1) / attn::kPfxRows;
+        const int tchunks = (sh + L.chunk_tiles - 1) / L.chunk_tiles;
+        for (int g = 0; g < num_kv_heads; ++g) {
+            for (int rc = 0; rc < chunks; ++rc) {
+                const int first_item = ni;
+                for (int tc = 0; tc < tchunks; ++tc) {
+                    const int t0 = tc * L.chunk_tiles;
+                    const int n = std::min(L.chunk_tiles, sh - t0);
+                    items[ni++] = make_int4(b + rc * attn::kPfxRows / G, std::min(attn::kPfxRows, m * G - rc * attn::kPfxRows),
+                                            g | (n << 16), t0);
+                }
+                // the sharers whose rows this chunk holds
+                for (int mi = rc * attn::kPfxRows / G; mi < std::min(m, (rc + 1) * attn::kPfxRows / G); ++mi) {
+                    const int sq = group_members[b + mi];
+                    targets[nt++] = make_int4(sq, g | (sh << 16), first_item,
+                                              tchunks | ((mi * G - rc * attn::kPfxRows) << 16));
+                }
+            }
+        }
+    }
+    if (ni != L.num_items || nt != L.num_targets) return PKV_ESTATE;
+    const cudaError_t e = cudaMemcpyAsync(static_cast<uint8_t*>(workspace) + L.skip_off, h, upload,
+                                          cudaMemcpyHostToDevice, as_stream(stream));
+    if (e != cudaSuccess) {
+        record_cuda_error(e);
+        return PKV_ECUDA;
+    }
+    return PKV_OK;
+}
+
+pkv_status pkv_attn_decode_cascade(const void* q, const void* k_cache, const void* v_cache,
+                                   const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                                   int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int num_blocks,
+                                   float scale, int num_groups, const int32_t* group_offsets,
+                                   const int32_t* group_shared_blocks, void* workspace, size_t workspace_bytes,
+                                   void* out, void* stream) {
+    attn::CascadeLayout CL;
+    pkv_status st = attn::cascade_layout(num_seqs, num_q_heads, num_kv_heads, num_groups, group_offsets,
+                                         group_shared_blocks, &CL);
+    if (st != PKV_OK) return st;
+    if (!workspace || workspace_bytes < CL.total) return PKV_EINVAL;
+    for (int gr = 0; gr < num_groups; ++gr)
+        if (group_shared_blocks[gr] > max_blocks_per_seq) return PKV_EINVAL;
+    attn::Launch L;
+    st = attn::prepare(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs, num_q_heads,
+                       num_kv_heads, head_dim, num_blocks, scale, 0, workspace, CL.decode_bytes, out, &L);
+    if (st != PKV_OK) return st;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    cudaStream_t s = as_stream(stream);
+    const attn::DeviceInfo dev = attn::device_info();
+    if (!dev.ok) return PKV_ECUDA;
+    attn::SideStream side;
+    if (CL.num_items > 0 && !attn::side_stream(&side)) return PKV_ECUDA;
+    auto cuda_ok = [](cudaError_t e) {
+        if (e != cudaSuccess) record_cuda_error(e);
+        return e == cudaSuccess;
+    };
+    if (CL.num_items > 0) {
+        // the prefix pass runs on the side stream, concurrently with the private pass
+        if (!cuda_ok(cudaEventRecord(side.fork, s)) || !cuda_ok(cudaStreamWaitEvent(side.stream, side.fork, 0)))
+            return PKV_ECUDA;
+        static std::once_flag once;
+        static cudaError_t attr_err = cudaSuccess;
+        std::call_once(once, [] {
+            attr_err = cudaFuncSetAttribute(attn::prefix_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            static_cast<int>(attn::kPfxSmem));
+        });
+        if (attr_err != cudaSuccess) {
+            record_cuda_error(attr_err);
+            return PKV_ECUDA;
+        }
+        attn::PrefixParams pp;
+        pp.q = static_cast<const __nv_bfloat16*>(q);
+        pp.block_tables = block_tables;
+        pp.max_blocks = max_blocks_per_seq;
+        pp.num_q_heads = num_q_heads;
+        pp.num_kv_heads = num_kv_heads;
+        pp.group = num_q_heads / num_kv_heads;
+        pp.num_blocks = num_blocks;
+        pp.scale_log2 = scale * 1.4426950408889634f;
+        pp.members = reinterpret_cast<const int32_t*>(ws + CL.members_off);
+        pp.items = reinterpret_cast<const int4*>(ws + CL.items_off);
+        pp.num_items = CL.num_items;
+        pp.err = L.prm.err;
+        pp.wpart = reinterpret_cast<float*>(ws + CL.wpart_off);
+        const int grid = std::min(CL.num_items, 3 * dev.sm_count);  // three CTAs fit on an SM
+        attn::prefix_kernel<<<grid, attn::kPfxThreads, attn::kPfxSmem, side.stream>>>(L.tm_k, L.tm_v, pp);
+        if (!cuda_ok(cudaGetLastError()) || !cuda_ok(cudaEventRecord(side.join, side.stream))) return PKV_ECUDA;
+    }
+    // the private pass: every sequence's tiles after its group's shared ones
+    L.prm.skip_tiles = reinterpret_cast<const int32_t*>(ws + CL.skip_off);
+    L.prm.side = reinterpret_cast<float*>(ws + CL.side_off);
+    L.grid = std::min(L.grid, attn::grid_for(num_seqs, PKV_BLOCK_TOKENS, true));
+    L.smem = attn::smem_bytes(num_seqs, true);
+    if (L.grid < 1) return PKV_ECUDA;
+    st = attn::launch(L, s, false);
+    if (CL.num_items > 0 && !cuda_ok(cudaStreamWaitEvent(s, side.join, 0))) return PKV_ECUDA;  // join first
+    if (st != PKV_OK || CL.num_targets == 0) return st;
+    attn::MergeParams mp;
+    mp.wpart = reinterpret_cast<const float*>(ws + CL.wpart_off);
+    mp.side = L.prm.side;
+    mp.out = static_cast<__nv_bfloat16*>(out);
+    mp.targets = reinterpret_cast<const int4*>(ws + CL.targets_off);
+    mp.context_lens = context_lens;
+    mp.cap_tokens = max_blocks_per_seq * PKV_BLOCK_TOKENS;
+    mp.num_targets = CL.num_targets;
+    mp.num_q_heads = num_q_heads;
+    mp.group = num_q_heads / num_kv_heads;
+    attn::cascade_merge_kernel<<<(CL.num_targets + 3) / 4, 128, 0, s>>>(mp);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        record_cuda_error(e);
+        return PKV_ECUDA;
+    }
+    return PKV_OK;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
 // Allocation-free variant of pkv_attn_decode.
 //
 // For callers that cannot allocate device memory themselves -- for example a
@@ -1302,6 +1939,8 @@ extern "C" pkv_status pkv_attn_decode_static(const void* q, const void* k_cache,
     prm.err = device_error ? device_error : reinterpret_cast<uint32_t*>(scratch);
     prm.counters = reinterpret_cast<int*>(scratch + attn::kWsHeader);
     prm.partials = reinterpret_cast<float*>(scratch + attn::kWsHeader + attn::kStaticCounterBytes);
+    prm.skip_tiles = nullptr;
+    prm.side = nullptr;
 
     attn::decode_kernel<PKV_BLOCK_TOKENS>
         <<<grid, attn::kThreads, attn::smem_bytes(num_seqs), as_stream(stream)>>>(tm_k, tm_v, prm);

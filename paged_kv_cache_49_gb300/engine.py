@@ -27,6 +27,32 @@ def bits_from_bf16(t: torch.Tensor) -> np.ndarray:
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
+def shared_prefix_groups(tables, context_lens, block_tokens: int = nat.BLOCK_TOKENS, min_members: int = 2):
+    """Groups of a batch's sequences that share leading blocks, for cascade
+    attention: sequences whose tables start with the same block form a group
+    (of at least min_members); its shared length is the longest table prefix
+    all members agree on, limited to the complete blocks of the shortest
+    member (a shared tile must be whole for every sharer). Host arithmetic on
+    the batch's block tables; returns [(member indices, shared blocks)]."""
+    tables = np.asarray(tables)
+    ctx = np.asarray(context_lens, dtype=np.int64)
+    by_first = {}
+    for s in range(len(ctx)):
+        if ctx[s] >= block_tokens:
+            by_first.setdefault(int(tables[s, 0]), []).append(s)
+    groups = []
+    for members in by_first.values():
+        if len(members) < min_members:
+            continue
+        limit = int(min(ctx[m] // block_tokens for m in members))
+        rows = tables[members, :limit]
+        agree = np.all(rows == rows[0], axis=0)
+        shared = limit if agree.all() else int(np.argmin(agree))
+        if shared >= 1:
+            groups.append((members, shared))
+    return groups
+
+
 @dataclass
 class StepBuffers:
     """Device inputs and output of one decode step (shapes fixed per batch)."""
