@@ -368,6 +368,11 @@ def run_ours(args):
               for _ in range(args.steps)]
     ev_copy = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(args.steps if sb.num_pairs else 0)]
+    # batches whose shared prefixes save enough reads: cascade attention too
+    cas = eng.cascade_for(sb)
+    cas_out = torch.empty_like(sb.out) if cas else None
+    ev_cas = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps if cas else 0)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -396,6 +401,11 @@ def run_ours(args):
             e0.record(stream)
             pkv.block_copy(eng.k_cache, eng.v_cache, sb.pairs, eng.error)
             e1.record(stream)
+        for i, (e0, e1) in enumerate(ev_cas):
+            flush(i + 4)
+            e0.record(stream)
+            cas.decode(sb.q, eng.k_cache, eng.v_cache, sb.tables, sb.ctx, w.scale, cas_out)
+            e1.record(stream)
         torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -410,8 +420,14 @@ def run_ours(args):
         t = [a.elapsed_time(b) for a, b in evs]
         return {"min": min(t), "median": statistics.median(t), "max": max(t)} if t else None
 
-    app_stats, copy_stats = stats_of(ev_app), stats_of(ev_copy)
-    launches = args.steps * (2 + (1 if sb.num_pairs else 0)) + args.steps + len(ev_app) + len(ev_copy)
+    app_stats, copy_stats, cas_stats = stats_of(ev_app), stats_of(ev_copy), stats_of(ev_cas)
+    launches = (args.steps * (2 + (1 if sb.num_pairs else 0)) + args.steps + len(ev_app) + len(ev_copy)
+                + 3 * len(ev_cas))
+    if cas is not None:
+        if cas.read_error():
+            raise RuntimeError("device error word set by the cascade attention")
+        if (cas_out.float() - sb.out.float()).abs().max().item() > 4e-2:
+            raise RuntimeError("cascade attention differs from the plain kernel")
     if eng.read_errors(sb):
         raise RuntimeError("device error word set during the timed steps")
 
@@ -466,6 +482,12 @@ def run_ours(args):
                 "kernel": "pkv::attn::decode_kernel", "algorithmic_bytes_per_launch": abytes,
                 "attn_ms": attn_s * 1e3, "attn_ms_min": min(attn_ms), "frac_of_nominal_8tbs": achieved / 8000.0,
                 "unique_kv_bytes_per_launch": ubytes, "unique_kv_gbs": ubytes / attn_s / 1e9}
+    if cas is not None:
+        cas_s = statistics.mean(a.elapsed_time(b) for a, b in ev_cas) * 1e-3
+        roofline["cascade"] = {"attn_ms": cas_s * 1e3, "groups": len(cas.groups),
+                               "saved_kv_bytes": pkv.cascade_saved_bytes(cas.groups, w.num_kv_heads),
+                               "logical_gbs": abytes / cas_s / 1e9, "unique_kv_gbs": ubytes / cas_s / 1e9,
+                               "frac_unique_of_measured": ubytes / cas_s / 1e9 / peak}
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         cpu = cpu_oracle_time(w)
@@ -480,7 +502,7 @@ def run_ours(args):
                    "parallelism": f"replicas x{world}"},
         "clocks": clk.summary(), "e2e": e2e, "gpu_launches": launches, "roofline": roofline,
         "timing_ms": {"step": step_stats, "attention_alone": attn_stats, "append_alone": app_stats,
-                      "block_copy_alone": copy_stats},
+                      "block_copy_alone": copy_stats, "attention_cascade": cas_stats},
         "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)

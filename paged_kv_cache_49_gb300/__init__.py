@@ -13,6 +13,7 @@ from ._native import (  # noqa: F401
     read_device_error,
 )
 from .engine import (  # noqa: F401
-    HostStep, PagedKVEngine, StepBuffers, bf16_from_bits, bits_from_bf16, shared_prefix_groups,
+    CASCADE_MIN_SAVED_BYTES, HostStep, PagedKVEngine, StepBuffers, bf16_from_bits, bits_from_bf16, cascade_saved_bytes,
+    shared_prefix_groups,
 )
 from .graphs import GraphedDecoder, default_buckets  # noqa: F401

@@ -1594,6 +1594,8 @@ pkv_status cascade_layout(int num_seqs, int num_q_heads, int num_kv_heads, int n
         passes += static_cast<long long>(num_kv_heads) * ((static_cast<long long>(m) * G + kPfxRows - 1) / kPfxRows) * sh;
         targets += static_cast<long long>(m) * num_kv_heads;
     }
+    const int total_members = num_groups > 0 ? group_offsets[num_groups] : 0;
+    if (total_members > num_seqs) return PKV_ERANGE;
     // Cut shared prefixes so that the prefix pass has about two items per
     // CTA slot: small batches get short items (more parallel reads), large
     // ones long items (fewer partials to merge).
@@ -1607,8 +1609,7 @@ pkv_status cascade_layout(int num_seqs, int num_q_heads, int num_kv_heads, int n
         const long long chunks = (static_cast<long long>(m) * G + kPfxRows - 1) / kPfxRows;
         items += num_kv_heads * chunks * ((group_shared_blocks[gr] + chunk - 1) / chunk);
     }
-    const int total_members = num_groups > 0 ? group_offsets[num_groups] : 0;
-    if (total_members > num_seqs || items > (1 << 28)) return PKV_ERANGE;
+    if (items > (1 << 28)) return PKV_ERANGE;
     const int grid = grid_for(num_seqs);
     if (grid < 1) return PKV_ECUDA;
     L->decode_bytes = align256(workspace_bytes(num_seqs, num_kv_heads, grid));
