@@ -299,7 +299,10 @@ pkv_status pkv_step_layout(int num_seqs, int num_q_heads, int num_kv_heads, int 
  * memory makes the copy asynchronous and fast) into device_staging (device,
  * layout.bytes, 256-byte aligned), the step itself reading its inputs from
  * there and writing attention rows to device_out (device, [num_seqs][Hq][D]
- * bf16), then one copy of those rows into host_out. Everything is enqueued
+ * bf16), then one copy of those rows into host_out. When host_out is pinned
+ * host memory the device can address (cudaHostAlloc / cudaHostRegister), the
+ * attention writes the rows there directly and device_out is not touched
+ * (it must still be a valid device pointer). Everything is enqueued
  * on `stream` and checked before anything is enqueued: host_packed must not
  * change, and host_out must not be read, until the stream has passed the
  * step (e.g. after cudaStreamSynchronize). This is the call through which a

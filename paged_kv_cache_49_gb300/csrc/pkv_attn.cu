@@ -1211,10 +1211,22 @@ pkv_status pkv_decode_step_host(const void* host_packed, void* device_staging, i
     const int32_t* pairs = num_pairs > 0 ? reinterpret_cast<const int32_t*>(d + lay.src_dst_pairs) : nullptr;
     const int32_t* tables = reinterpret_cast<const int32_t*>(d + lay.block_tables);
     const int32_t* ctx = reinterpret_cast<const int32_t*>(d + lay.context_lens);
+    // Output rows go straight to host_out when it is pinned host memory the
+    // device can address (the kernel's stores cross the host link as it
+    // finishes pieces), else to device_out and back in one copy.
+    void* direct = nullptr;
+    {
+        cudaPointerAttributes pa;
+        if (cudaPointerGetAttributes(&pa, host_out) == cudaSuccess) {
+            if (pa.type == cudaMemoryTypeHost && pa.devicePointer) direct = pa.devicePointer;
+        } else {
+            cudaGetLastError();  // pageable memory: not an error here
+        }
+    }
     attn::Launch L;
     st = check_step(k_new, v_new, slots, num_seqs, pairs, num_pairs, k_cache, v_cache, num_blocks, q, tables,
                     max_blocks_per_seq, ctx, num_seqs, num_q_heads, num_kv_heads, head_dim, scale, num_ctas,
-                    workspace, workspace_bytes, device_out, &L);
+                    workspace, workspace_bytes, direct ? direct : device_out, &L);
     if (st != PKV_OK) return st;
     cudaStream_t s = as_stream(stream);
     cudaError_t e = cudaMemcpyAsync(device_staging, host_packed, lay.bytes, cudaMemcpyHostToDevice, s);
@@ -1224,7 +1236,7 @@ pkv_status pkv_decode_step_host(const void* host_packed, void* device_staging, i
     }
     st = enqueue_step(L, k_new, v_new, slots, num_seqs, pairs, num_pairs, k_cache, v_cache, num_blocks,
                       num_kv_heads, head_dim, device_error, stream);
-    if (st != PKV_OK) return st;
+    if (st != PKV_OK || direct) return st;
     e = cudaMemcpyAsync(host_out, device_out, static_cast<size_t>(num_seqs) * num_q_heads * head_dim * 2,
                         cudaMemcpyDeviceToHost, s);
     if (e != cudaSuccess) {

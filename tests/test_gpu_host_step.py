@@ -58,3 +58,25 @@ def test_host_step_matches_device_step(pkv, name):
     out_again = step.out_host.clone()
     assert torch.equal(out_again, out_dev.cpu())
     assert torch.equal(host.k_cache, dev.k_cache) and torch.equal(host.v_cache, dev.v_cache)
+
+
+def test_host_step_output_to_pageable_memory(pkv):
+    """Pinned host_out is written by the kernel directly; pageable host_out
+    goes through device_out and one copy. Both give the same rows."""
+    w = make_workload("tiny")
+    q, k, v = w.step_inputs()
+    eng = _engine(pkv, w)
+    slots, pairs = eng.bm.prepare_append(w.batch)
+    width = 16
+    tables, ctx = eng.bm.batch_tables(w.batch, width)
+    step = pkv.HostStep(eng, len(w.batch), width, max_pairs=4)
+    step.pack(pkv.bf16_from_bits(q), pkv.bf16_from_bits(k), pkv.bf16_from_bits(v), slots, tables, ctx, pairs)
+    step.run(w.scale)
+    torch.cuda.synchronize()
+    pinned = step.out_host.clone()
+    pageable = torch.empty_like(step.out_host)  # not pinned
+    assert not pageable.is_pinned()
+    pkv.decode_step_host(step.host, step.staging, step.num_pairs, eng.k_cache, eng.v_cache, width, len(w.batch),
+                         w.num_q_heads, w.scale, step.workspace, step.out_dev, pageable, eng.error)
+    torch.cuda.synchronize()
+    assert torch.equal(pinned, pageable) and torch.equal(step.out_dev.cpu(), pageable)
