@@ -1273,8 +1273,10 @@ namespace attn {
 constexpr int kPfxRows = 32;     // query rows per prefix item: 8 per consumer warp
 constexpr int kPfxTiles = 64;    // shared tiles per prefix item at most
 constexpr int kPfxThreads = kConsumers + 32;
-constexpr int kPfxOffBar = kStages * kStageBytes;
-constexpr size_t kPfxSmem = 1024 + kPfxOffBar + 2 * kStages * 8 + 64;
+constexpr int kPfxStages = 8;       // ring depth of the prefix pass
+constexpr int kPfxCtasPerSm = 3;    // resident prefix CTAs per SM (shared memory and registers)
+constexpr int kPfxOffBar = kPfxStages * kStageBytes;
+constexpr size_t kPfxSmem = 1024 + kPfxOffBar + 2 * kPfxStages * 8 + 64;
 
 struct PrefixParams {
     const __nv_bfloat16* q;
@@ -1293,7 +1295,7 @@ struct PrefixParams {
     float* wpart;            // [num_items][kPfxRows][kORow]
 };
 
-__global__ void __launch_bounds__(kPfxThreads, 1)
+__global__ void __launch_bounds__(kPfxThreads, kPfxCtasPerSm)
 prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
               const PrefixParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -1305,14 +1307,14 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     const int Hkv = p.num_kv_heads;
     const uint32_t bar0 = smem_u32(smem + kPfxOffBar);
     auto full_bar = [&](int i) { return bar0 + 8u * i; };
-    auto empty_bar = [&](int i) { return bar0 + 8u * (kStages + i); };
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kPfxOffBar + 2 * kStages * 8);
+    auto empty_bar = [&](int i) { return bar0 + 8u * (kPfxStages + i); };
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kPfxOffBar + 2 * kPfxStages * 8);
     if (warp == kProducerWarp && lane == 0) {
         prefetch_tensormap(&tm_k);
         prefetch_tensormap(&tm_v);
     }
     if (tid == 0) {
-        for (int i = 0; i < kStages; ++i) {
+        for (int i = 0; i < kPfxStages; ++i) {
             mbar_init(full_bar(i), 1);
             mbar_init(empty_bar(i), kConsumerWarps);  // every consumer warp reads every stage
         }
@@ -1352,14 +1354,14 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                         tma_load_2d(dst + kBlockBytes + kHalfBytes, &tm_v, 64, ya, fb, policy);
                         ++issued;
                     }
-                    if (++stage == kStages) { stage = 0; sphase ^= 1u; }
+                    if (++stage == kPfxStages) { stage = 0; sphase ^= 1u; }
                 }
             }
         }
         if (lane == 0) {  // no copy may land after the CTA exits (bounded waits)
             volatile int never = 0;
-            for (int i = max(0, issued - kStages); i < issued; ++i)
-                mbar_wait(full_bar(i % kStages), static_cast<uint32_t>((i / kStages) & 1), &never, nullptr);
+            for (int i = max(0, issued - kPfxStages); i < issued; ++i)
+                mbar_wait(full_bar(i % kPfxStages), static_cast<uint32_t>((i / kPfxStages) & 1), &never, nullptr);
         }
         return;
     }
@@ -1374,7 +1376,7 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     const uint32_t v_row_off = static_cast<uint32_t>((lane & 7) + ((v_mat >> 1) << 3)) * 128u;
     const int v_sw = lane & 7;
     const float NEG_INF = -INFINITY;
-    int gi = 0;  // the CTA's tile count so far: stage gi % kStages
+    int gi = 0;  // the CTA's tile count so far: stage gi % kPfxStages
     for (int it = blockIdx.x; it < p.num_items; it += gridDim.x) {
         const int4 item = p.items[it];
         const int g = item.z & 0xffff, n = item.z >> 16;
@@ -1396,8 +1398,8 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
 #pragma unroll
         for (int j = 0; j < 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
         for (int t = 0; t < n; ++t, ++gi) {
-            const int st = gi % kStages;
-            mbar_wait(full_bar(st), static_cast<uint32_t>((gi / kStages) & 1), abort_flag, p.err);
+            const int st = gi % kPfxStages;
+            mbar_wait(full_bar(st), static_cast<uint32_t>((gi / kPfxStages) & 1), abort_flag, p.err);
             const uint32_t sk = smem_u32(smem + st * kStageBytes);
             const uint32_t sv = sk + kBlockBytes;
             float sa[4] = {0.f, 0.f, 0.f, 0.f};
@@ -1608,13 +1610,16 @@ pkv_status cascade_layout(int num_seqs, int num_q_heads, int num_kv_heads, int n
     }
     const int total_members = num_groups > 0 ? group_offsets[num_groups] : 0;
     if (total_members > num_seqs) return PKV_ERANGE;
-    // Cut shared prefixes so that the prefix pass has about two items per
-    // CTA slot: small batches get short items (more parallel reads), large
-    // ones long items (fewer partials to merge).
+    // Cut shared prefixes into items of 8..64 tiles, aiming at about one item
+    // per two CTA slots: a small batch gets short items (parallel reads), a
+    // large one long items (fewer partials to merge, and fewer CTAs taken
+    // from the concurrent private pass). Measured on a 16 x 8 fan-out: 64-tile
+    // items 76 us, 21-tile items 80 us; on a 7-request group 8-tile items
+    // 32 us, 64-tile items 55 us.
     const DeviceInfo dev = device_info();
     if (!dev.ok) return PKV_ECUDA;
-    const long long slots = 3ll * dev.sm_count;
-    int chunk = static_cast<int>(std::min<long long>(kPfxTiles, std::max<long long>(8, (passes + 2 * slots - 1) / (2 * slots))));
+    const long long slots = static_cast<long long>(kPfxCtasPerSm) * dev.sm_count;
+    int chunk = static_cast<int>(std::min<long long>(kPfxTiles, std::max<long long>(8, (2 * passes + slots - 1) / slots)));
     L->chunk_tiles = chunk;
     for (int gr = 0; gr < num_groups; ++gr) {
         const int m = group_offsets[gr + 1] - group_offsets[gr];
@@ -1812,7 +1817,7 @@ pkv_status pkv_attn_decode_cascade(const void* q, const void* k_cache, const voi
         pp.num_items = CL.num_items;
         pp.err = L.prm.err;
         pp.wpart = reinterpret_cast<float*>(ws + CL.wpart_off);
-        const int grid = std::min(CL.num_items, 3 * dev.sm_count);  // three CTAs fit on an SM
+        const int grid = std::min(CL.num_items, attn::kPfxCtasPerSm * dev.sm_count);
         attn::prefix_kernel<<<grid, attn::kPfxThreads, attn::kPfxSmem, side.stream>>>(L.tm_k, L.tm_v, pp);
         if (!cuda_ok(cudaGetLastError()) || !cuda_ok(cudaEventRecord(side.join, side.stream))) return PKV_ECUDA;
     }
