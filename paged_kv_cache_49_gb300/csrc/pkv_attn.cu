@@ -234,7 +234,10 @@ struct PieceWalk {
 // kBT: tokens per cache block (8, 16, 32 or 64). A 16-token tile is rows
 // [(t mod kBT/16) * 16, +16) of block table[t / (kBT/16)] when kBT >= 16, and
 // the two 8-row blocks table[2t], table[2t + 1] when kBT == 8.
-template <int kBT>
+// kSkip: the private pass of cascade attention (per-sequence skipped tiles,
+// fp32 results for grouped sequences); a separate instantiation, so that the
+// plain kernel carries none of its branches.
+template <int kBT, bool kSkip = false>
 __global__ void __launch_bounds__(kThreads, 2)
 decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
               const Params p) {
@@ -249,7 +252,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
 
     int* scan = reinterpret_cast<int*>(smem + kOffScan);
     uint8_t* tail = smem + kOffScan + 4 * static_cast<size_t>(B);  // tokens in each sequence's last tile
-    int* skip = p.skip_tiles ? reinterpret_cast<int*>(smem + skip_offset(B)) : nullptr;
+    int* skip = kSkip ? reinterpret_cast<int*>(smem + skip_offset(B)) : nullptr;
     auto skipped = [&](int s) { return skip ? skip[s] : 0; };
     int* misc = reinterpret_cast<int*>(smem + kOffMisc);
     volatile int* abort_flag = misc;  // misc[0]
@@ -514,7 +517,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             // The pair's finished result for head h: a bf16 output row, or, for
             // a sequence whose leading tiles another pass covers, its
             // unnormalised fp32 result for the cascade merge.
-            const bool to_side = p.side && skipped(s) > 0;
+            const bool to_side = kSkip && skipped(s) > 0;
             float* side_base = to_side ? p.side + (static_cast<size_t>(s) * p.num_q_heads + static_cast<size_t>(g) * G) * kORow
                                        : nullptr;
             auto emit = [&](int h, float4 acc, float M, float L) {
@@ -909,7 +912,10 @@ DeviceInfo device_info() {
     for (int bt : {8, 16, 32, 64})
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(kernel_for(bt), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(smem_bytes(PKV_ATTN_MAX_SEQS, true)));
+                                     static_cast<int>(smem_bytes(PKV_ATTN_MAX_SEQS)));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(decode_kernel<PKV_BLOCK_TOKENS, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem_bytes(PKV_ATTN_MAX_SEQS, true)));
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) {
         record_cuda_error(e);
@@ -924,7 +930,8 @@ DeviceInfo device_info() {
 // CTA per SM instead of two). 0 on error.
 int grid_for(int num_seqs, int block_tokens = PKV_BLOCK_TOKENS, bool skip = false) {
     const DeviceInfo d = device_info();
-    const KernelFn fn = kernel_for(block_tokens);
+    const KernelFn fn = skip ? (block_tokens == PKV_BLOCK_TOKENS ? decode_kernel<PKV_BLOCK_TOKENS, true> : nullptr)
+                             : kernel_for(block_tokens);
     if (!d.ok || !fn) return 0;
     // Cached per (device, block size, shared memory size), so that a call
     // made while a stream is being captured into a graph issues no CUDA query.
@@ -933,7 +940,7 @@ int grid_for(int num_seqs, int block_tokens = PKV_BLOCK_TOKENS, bool skip = fals
     int dev = 0;
     cudaGetDevice(&dev);
     const size_t smem = smem_bytes(num_seqs, skip);
-    const std::pair<int, size_t> key{dev * 128 + block_tokens, smem};
+    const std::pair<int, size_t> key{(dev * 128 + block_tokens) * 2 + (skip ? 1 : 0), smem};
     {
         std::lock_guard<std::mutex> lock(mu);
         auto it = cache.find(key);
@@ -1824,6 +1831,7 @@ pkv_status pkv_attn_decode_cascade(const void* q, const void* k_cache, const voi
     // the private pass: every sequence's tiles after its group's shared ones
     L.prm.skip_tiles = reinterpret_cast<const int32_t*>(ws + CL.skip_off);
     L.prm.side = reinterpret_cast<float*>(ws + CL.side_off);
+    L.fn = attn::decode_kernel<PKV_BLOCK_TOKENS, true>;
     L.grid = std::min(L.grid, attn::grid_for(num_seqs, PKV_BLOCK_TOKENS, true));
     L.smem = attn::smem_bytes(num_seqs, true);
     if (L.grid < 1) return PKV_ECUDA;
