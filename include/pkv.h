@@ -169,8 +169,9 @@ pkv_status pkv_attn_workspace_init(void* workspace, size_t workspace_bytes, void
  * Limits: head_dim == 128, num_q_heads % num_kv_heads == 0,
  * num_q_heads / num_kv_heads <= 8, 1 <= num_seqs <= 4096,
  * num_blocks * num_kv_heads * 16 < 2^31, num_seqs * max_blocks_per_seq < 2^31
- * and num_kv_heads * num_seqs * max_blocks_per_seq * (block tokens / 16)
- * < 2^30 (PKV_ERANGE otherwise). A block id outside [0, num_blocks)
+ * and num_kv_heads * num_seqs * (ceil(max_blocks_per_seq * block tokens / 16)
+ * + 3) < 2^30 (PKV_ERANGE otherwise; the + 3 is the work partition's charge
+ * per (sequence, KV head) run). A block id outside [0, num_blocks)
  * is never dereferenced: block 0 is read in its place and PKV_DEVERR_BLOCK_ID
  * is set (the output is then invalid); context_lens above
  * 16 * max_blocks_per_seq are clamped and set PKV_DEVERR_CONTEXT.

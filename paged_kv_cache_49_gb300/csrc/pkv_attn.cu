@@ -71,6 +71,11 @@ static_assert(kStages % kConsumerWarps == 0, "each stage must map to one consume
 static_assert((kConsumerWarps & (kConsumerWarps - 1)) == 0, "consumer warp count is a power of two");
 constexpr int kQSlots = 2;
 constexpr int kMergeSlots = 2;
+// Work partition cost of one (sequence, KV head) run beyond its tiles, in
+// tiles: what a piece's fixed work (its query rows, the hand-over between
+// consumer warps, the merge warp's combine and any cross-CTA merge) costs a
+// CTA, next to streaming one 8 KB tile at its share of HBM bandwidth.
+constexpr int kPieceCost = 3;
 constexpr int kHalfBytes = kTok * 64 * 2;  // one 16 x 64 bf16 box
 constexpr int kBlockBytes = 2 * kHalfBytes;  // one K (or V) block of one KV head
 constexpr int kStageBytes = 2 * kBlockBytes;
@@ -152,8 +157,8 @@ __device__ __forceinline__ int find_seq(const int* scan, int n, int t) {
     return lo;
 }
 
-// Positions on the line are 32-bit: the host rejects launches whose line
-// could reach 2^30 tiles.
+// Positions on the line, and cost positions of the work partition, are
+// 32-bit: the host rejects launches whose line could reach 2^30 cost units.
 __device__ __forceinline__ Cursor locate(const int* scan, int n, int hkv, int x) {
     Cursor c;
     c.s = find_seq(scan, n, x / hkv);
@@ -162,6 +167,28 @@ __device__ __forceinline__ Cursor locate(const int* scan, int n, int hkv, int x)
     c.g = off / nb;
     c.blk = off - c.g * nb;
     return c;
+}
+
+// The work partition deals out cost, not tiles: tile x of run r = s * hkv + g
+// sits at cost position x + kPieceCost * r, so that each run is followed by a
+// gap of kPieceCost positions that hold no tile. Sequence s's runs start at
+// cost hkv * (scan[s-1] + kPieceCost * s), each run taking nb + kPieceCost
+// positions. Returns the first tile whose cost position is >= y (total when
+// none is).
+__device__ __forceinline__ int line_at(const int* scan, int n, int hkv, int y, int total, int cost_total) {
+    if (y >= cost_total) return total;
+    const int t = y / hkv;
+    int lo = 0, hi = n - 1;  // smallest s with scan[s] + kPieceCost * (s + 1) > t
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (scan[mid] + kPieceCost * (mid + 1) > t) hi = mid; else lo = mid + 1;
+    }
+    const int nb = run_blocks(scan, lo);
+    const int before = scan[lo] - nb;  // tiles of one head before sequence lo
+    const int off = y - hkv * (before + kPieceCost * lo);
+    const int g = off / (nb + kPieceCost);
+    const int w = off - g * (nb + kPieceCost);
+    return hkv * before + g * nb + min(w, nb);
 }
 
 __device__ __forceinline__ void advance(Cursor& c, const int* scan, int n, int hkv, int len) {
@@ -332,10 +359,14 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         __syncthreads();
     }
 
+    // CTA b takes the tiles whose cost position lies in [b, b + 1) * cchunk:
+    // equal shares of tiles plus per-run overhead, so that a CTA whose range
+    // is cut into many short pieces streams fewer tiles.
     const int total = Hkv * scan[B - 1];
-    const int chunk = (total + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
-    const int range_lo = static_cast<int>(min(static_cast<long long>(total), static_cast<long long>(blockIdx.x) * chunk));
-    const int range_hi = range_lo + min(chunk, total - range_lo);
+    const int cost_total = Hkv * (scan[B - 1] + kPieceCost * B);
+    const int cchunk = (cost_total + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
+    const int range_lo = line_at(scan, B, Hkv, static_cast<int>(blockIdx.x) * cchunk, total, cost_total);
+    const int range_hi = line_at(scan, B, Hkv, static_cast<int>(blockIdx.x + 1) * cchunk, total, cost_total);
 
     // The merge warp, idle until the first piece ends, warms L2 with the
     // block-table entries and query rows of this CTA's range -- two
@@ -502,9 +533,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             for (int w = 0; w < kConsumerWarps; ++w)
                 if (((w - gidx0 % kConsumerWarps) & (kConsumerWarps - 1)) < pc.len) owners |= 1u << w;
             gidx0 += pc.len;
-            const int seg_start = Hkv * (scan[s] - nb) + g * nb;
-            const int i0 = static_cast<int>(seg_start / chunk);
-            const int i1 = static_cast<int>((seg_start + nb - 1) / chunk);
+            // the CTAs holding pieces of this pair, from its cost positions
+            const int seg_cost = Hkv * (scan[s] - nb) + g * nb + kPieceCost * (s * Hkv + g);
+            const int i0 = seg_cost / cchunk;
+            const int i1 = (seg_cost + nb - 1) / cchunk;
             const int pieces = i1 - i0 + 1;
             const int ms = piece % kMergeSlots;
             mbar_wait(mfull_bar(ms), static_cast<uint32_t>((piece / kMergeSlots) & 1), abort_flag, p.err);
@@ -513,7 +545,11 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             const float* ml = sm_l + ms * kMergeMLFloats;
             __nv_bfloat16* out_base =
                 p.out + (static_cast<size_t>(s) * p.num_q_heads + static_cast<size_t>(g) * G) * kDim + d0;
-            float* part = p.partials + (static_cast<size_t>(blockIdx.x) * 2 + (pc.start == range_lo ? 0 : 1)) * kPartialFloats;
+            // Partial slots: a CTA holds at most two split pieces, one that
+            // continues into the next CTA (slot 1) and one that ends a pair
+            // begun in an earlier CTA (slot 0).
+            const bool continues = pc.start + pc.len == range_hi && pc.blk + pc.len < nb;
+            float* part = p.partials + (static_cast<size_t>(blockIdx.x) * 2 + (continues ? 1 : 0)) * kPartialFloats;
             // The pair's finished result for head h: a bf16 output row, or, for
             // a sequence whose leading tiles another pass covers, its
             // unnormalised fp32 result for the cascade merge.
@@ -602,7 +638,6 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 old = __shfl_sync(0xffffffffu, old, 0);
                 __syncwarp();
                 if (old == pieces - 1) {  // last piece of the pair to finish: merge them all
-                    const int slot0 = (seg_start == i0 * chunk) ? 0 : 1;
                     // An online log-sum-exp pass over the pieces, four pieces
                     // (and four heads) at a time: each batch's loads are all
                     // issued before any of them is used, so a pair split into
@@ -625,7 +660,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
 #pragma unroll
                                 for (int k = 0; k < 4; ++k) {
                                     const float* pi = p.partials +
-                                        (static_cast<size_t>(i + k) * 2 + (i + k == i0 ? slot0 : 0)) * kPartialFloats;
+                                        (static_cast<size_t>(i + k) * 2 + (i + k == i1 ? 0 : 1)) * kPartialFloats;
 #pragma unroll
                                     for (int h = 0; h < 4; ++h) {
                                         if (i + k <= i1 && hb + h < G) {
@@ -983,7 +1018,7 @@ pkv_status prepare(const void* q, const void* k_cache, const void* v_cache, cons
     if (static_cast<long long>(num_blocks) * num_kv_heads * block_tokens >= (1ll << 31) ||
         static_cast<long long>(num_seqs) * max_blocks_per_seq >= (1ll << 31) ||
         static_cast<long long>(max_blocks_per_seq) * block_tokens >= (1ll << 31) ||
-        static_cast<long long>(num_kv_heads) * num_seqs * max_blocks_per_seq * block_tokens / kTok >= (1ll << 30))
+        static_cast<long long>(num_kv_heads) * num_seqs * ((static_cast<long long>(max_blocks_per_seq) * block_tokens + kTok - 1) / kTok + kPieceCost) >= (1ll << 30))
         return PKV_ERANGE;
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
         (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
@@ -1925,7 +1960,7 @@ extern "C" pkv_status pkv_attn_decode_static(const void* q, const void* k_cache,
     if (static_cast<long long>(num_blocks) * num_kv_heads * PKV_BLOCK_TOKENS >= (1ll << 31) ||
         static_cast<long long>(num_seqs) * max_blocks_per_seq >= (1ll << 31) ||
         static_cast<long long>(max_blocks_per_seq) * PKV_BLOCK_TOKENS >= (1ll << 31) ||
-        static_cast<long long>(num_kv_heads) * num_seqs * max_blocks_per_seq >= (1ll << 30))
+        static_cast<long long>(num_kv_heads) * num_seqs * (max_blocks_per_seq + attn::kPieceCost) >= (1ll << 30))
         return PKV_ERANGE;
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return PKV_EINVAL;
     const int auto_grid = attn::grid_for(num_seqs);
