@@ -70,7 +70,6 @@ constexpr int kStages = 8;
 static_assert(kStages % kConsumerWarps == 0, "each stage must map to one consumer warp");
 static_assert((kConsumerWarps & (kConsumerWarps - 1)) == 0, "consumer warp count is a power of two");
 constexpr int kQSlots = 2;
-constexpr int kMergeSlots = 2;
 // Work partition cost of one (sequence, KV head) run beyond its tiles, in
 // tiles: what a piece's fixed work (its query rows, the hand-over between
 // consumer warps, the merge warp's combine and any cross-CTA merge) costs a
@@ -88,21 +87,35 @@ constexpr int kMergeMLFloats = kConsumerWarps * kMaxG;
 constexpr int kOffStages = 0;
 constexpr int kOffQ = kOffStages + kStages * kStageBytes;
 constexpr int kOffO = kOffQ + kQSlots * kQBytes;
-constexpr int kOffM = kOffO + kMergeSlots * kMergeOFloats * 4;
-constexpr int kOffL = kOffM + kMergeSlots * kMergeMLFloats * 4;
-constexpr int kOffBar = kOffL + kMergeSlots * kMergeMLFloats * 4;
-constexpr int kNumBars = 2 * kStages + 2 * kQSlots + 2 * kMergeSlots;
-constexpr int kOffMisc = kOffBar + kNumBars * 8;
-constexpr int kOffScan = kOffMisc + 64;
+// The rest of the layout depends on the number of merge slots S (consumer
+// warps' piece states waiting for the merge warp): 2 lets the consumers
+// finish a piece while the merge warp combines the previous one; 1 saves
+// 16.9 KB, which keeps two CTAs per SM for batches whose prefix sums would
+// otherwise push a CTA past half of the SM's shared memory.
+template <int S>
+struct Layout {
+    static constexpr int kOffM = kOffO + S * kMergeOFloats * 4;
+    static constexpr int kOffL = kOffM + S * kMergeMLFloats * 4;
+    static constexpr int kOffBar = kOffL + S * kMergeMLFloats * 4;
+    static constexpr int kNumBars = 2 * kStages + 2 * kQSlots + 2 * S;
+    static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+    static constexpr int kOffScan = kOffMisc + 64;
+};
+
+__host__ __device__ constexpr int off_scan(int slots) {
+    return slots == 1 ? Layout<1>::kOffScan : Layout<2>::kOffScan;
+}
 
 // Dynamic shared memory: the fixed part, the prefix sum (4 bytes per
 // sequence), each sequence's last-tile token count (1 byte per sequence) and,
 // when leading tiles are skipped (the private pass of cascade attention), each
 // sequence's skipped tile count (4 bytes per sequence).
-__host__ __device__ constexpr size_t skip_offset(int num_seqs) { return (kOffScan + 5 * static_cast<size_t>(num_seqs) + 3) & ~size_t(3); }
-constexpr size_t smem_bytes(int num_seqs, bool skip = false) {
-    return 1024 + (skip ? skip_offset(num_seqs) + 4 * static_cast<size_t>(num_seqs)
-                        : kOffScan + 5 * static_cast<size_t>(num_seqs));
+__host__ __device__ constexpr size_t skip_offset(int num_seqs, int slots) {
+    return (off_scan(slots) + 5 * static_cast<size_t>(num_seqs) + 3) & ~size_t(3);
+}
+constexpr size_t smem_bytes(int num_seqs, bool skip, int slots) {
+    return 1024 + (skip ? skip_offset(num_seqs, slots) + 4 * static_cast<size_t>(num_seqs)
+                        : off_scan(slots) + 5 * static_cast<size_t>(num_seqs));
 }
 
 constexpr size_t kWsHeader = 256;
@@ -263,8 +276,8 @@ struct PieceWalk {
 // the two 8-row blocks table[2t], table[2t + 1] when kBT == 8.
 // kSkip: the private pass of cascade attention (per-sequence skipped tiles,
 // fp32 results for grouped sequences); a separate instantiation, so that the
-// plain kernel carries none of its branches.
-template <int kBT, bool kSkip = false>
+// plain kernel carries none of its branches. kSlots: merge slots (1 or 2).
+template <int kBT, bool kSkip, int kSlots>
 __global__ void __launch_bounds__(kThreads, 2)
 decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
               const Params p) {
@@ -277,23 +290,24 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     const int Hkv = p.num_kv_heads;
     const int G = p.group;
 
-    int* scan = reinterpret_cast<int*>(smem + kOffScan);
-    uint8_t* tail = smem + kOffScan + 4 * static_cast<size_t>(B);  // tokens in each sequence's last tile
-    int* skip = kSkip ? reinterpret_cast<int*>(smem + skip_offset(B)) : nullptr;
+    using LY = Layout<kSlots>;
+    int* scan = reinterpret_cast<int*>(smem + LY::kOffScan);
+    uint8_t* tail = smem + LY::kOffScan + 4 * static_cast<size_t>(B);  // tokens in each sequence's last tile
+    int* skip = kSkip ? reinterpret_cast<int*>(smem + skip_offset(B, kSlots)) : nullptr;
     auto skipped = [&](int s) { return skip ? skip[s] : 0; };
-    int* misc = reinterpret_cast<int*>(smem + kOffMisc);
+    int* misc = reinterpret_cast<int*>(smem + LY::kOffMisc);
     volatile int* abort_flag = misc;  // misc[0]
     int* warp_tot = misc + 8;         // misc[8 .. 8 + kThreads / 32)
     float* sm_o = reinterpret_cast<float*>(smem + kOffO);
-    float* sm_m = reinterpret_cast<float*>(smem + kOffM);
-    float* sm_l = reinterpret_cast<float*>(smem + kOffL);
-    const uint32_t bar0 = smem_u32(smem + kOffBar);
+    float* sm_m = reinterpret_cast<float*>(smem + LY::kOffM);
+    float* sm_l = reinterpret_cast<float*>(smem + LY::kOffL);
+    const uint32_t bar0 = smem_u32(smem + LY::kOffBar);
     auto full_bar = [&](int i) { return bar0 + 8u * i; };
     auto empty_bar = [&](int i) { return bar0 + 8u * (kStages + i); };
     auto qfull_bar = [&](int i) { return bar0 + 8u * (2 * kStages + i); };
     auto qempty_bar = [&](int i) { return bar0 + 8u * (2 * kStages + kQSlots + i); };
     auto mfull_bar = [&](int i) { return bar0 + 8u * (2 * kStages + 2 * kQSlots + i); };
-    auto mempty_bar = [&](int i) { return bar0 + 8u * (2 * kStages + 2 * kQSlots + kMergeSlots + i); };
+    auto mempty_bar = [&](int i) { return bar0 + 8u * (2 * kStages + 2 * kQSlots + kSlots + i); };
 
     if (warp == kProducerWarp && lane == 0) {  // fetch the TMA descriptors while the plan runs
         prefetch_tensormap(&tm_k);
@@ -308,7 +322,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             mbar_init(qfull_bar(i), 1);
             mbar_init(qempty_bar(i), kConsumerWarps);
         }
-        for (int i = 0; i < kMergeSlots; ++i) {
+        for (int i = 0; i < kSlots; ++i) {
             mbar_init(mfull_bar(i), kConsumers);
             mbar_init(mempty_bar(i), 32);
         }
@@ -538,8 +552,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             const int i0 = seg_cost / cchunk;
             const int i1 = (seg_cost + nb - 1) / cchunk;
             const int pieces = i1 - i0 + 1;
-            const int ms = piece % kMergeSlots;
-            mbar_wait(mfull_bar(ms), static_cast<uint32_t>((piece / kMergeSlots) & 1), abort_flag, p.err);
+            const int ms = piece % kSlots;
+            mbar_wait(mfull_bar(ms), static_cast<uint32_t>((piece / kSlots) & 1), abort_flag, p.err);
             const float* mo = sm_o + ms * kMergeOFloats;
             const float* mm = sm_m + ms * kMergeMLFloats;
             const float* ml = sm_l + ms * kMergeMLFloats;
@@ -850,7 +864,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         // ---- hand this warp's state for the piece to the merge warp ----
         // (a warp without blocks in the piece writes nothing: the merge warp
         // knows from the piece's geometry which warps contributed)
-        const int ms = piece % kMergeSlots;
+        const int ms = piece % kSlots;
         if (mine) {
 #pragma unroll
             for (int off = 4; off < 32; off <<= 1) {
@@ -858,7 +872,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 l1 += __shfl_xor_sync(0xffffffffu, l1, off);
             }
         }
-        mbar_wait(mempty_bar(ms), static_cast<uint32_t>(((piece / kMergeSlots) & 1) ^ 1), abort_flag, p.err);
+        mbar_wait(mempty_bar(ms), static_cast<uint32_t>(((piece / kSlots) & 1) ^ 1), abort_flag, p.err);
         if (mine) {
             float* o0 = sm_o + ms * kMergeOFloats + (warp * kMaxG + 2 * c) * kORow + r;
             float* o1 = o0 + kORow;
@@ -917,15 +931,22 @@ bool make_cache_map(CUtensorMap* map, const void* base, int num_blocks, int hkv,
 
 using KernelFn = void (*)(CUtensorMap, CUtensorMap, Params);
 
-// The instantiation for a block size (8, 16, 32 or 64 tokens), else null.
-KernelFn kernel_for(int block_tokens) {
+// The instantiation for a block size (8, 16, 32 or 64 tokens), skipped tiles
+// (16-token blocks only) and merge slots (1 or 2), else null.
+template <int S>
+KernelFn kernel_for_slots(int block_tokens, bool skip) {
+    if (skip) return block_tokens == PKV_BLOCK_TOKENS ? decode_kernel<PKV_BLOCK_TOKENS, true, S> : nullptr;
     switch (block_tokens) {
-        case 8: return decode_kernel<8>;
-        case 16: return decode_kernel<16>;
-        case 32: return decode_kernel<32>;
-        case 64: return decode_kernel<64>;
+        case 8: return decode_kernel<8, false, S>;
+        case 16: return decode_kernel<16, false, S>;
+        case 32: return decode_kernel<32, false, S>;
+        case 64: return decode_kernel<64, false, S>;
         default: return nullptr;
     }
+}
+
+KernelFn kernel_for(int block_tokens, bool skip, int slots) {
+    return slots == 1 ? kernel_for_slots<1>(block_tokens, skip) : kernel_for_slots<2>(block_tokens, skip);
 }
 
 struct DeviceInfo {
@@ -933,7 +954,7 @@ struct DeviceInfo {
     int sm_count = 0;
 };
 
-// Per device, once: allow the kernel its largest dynamic shared memory.
+// Per device, once: allow every instantiation its largest dynamic shared memory.
 DeviceInfo device_info() {
     static std::mutex mu;
     static std::vector<DeviceInfo> cache;
@@ -944,13 +965,14 @@ DeviceInfo device_info() {
     DeviceInfo& d = cache[dev];
     if (d.ok) return d;
     cudaError_t e = cudaSuccess;
-    for (int bt : {8, 16, 32, 64})
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(kernel_for(bt), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(smem_bytes(PKV_ATTN_MAX_SEQS)));
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(decode_kernel<PKV_BLOCK_TOKENS, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(smem_bytes(PKV_ATTN_MAX_SEQS, true)));
+    for (int slots : {1, 2})
+        for (int bt : {8, 16, 32, 64})
+            for (bool skip : {false, true}) {
+                const KernelFn fn = kernel_for(bt, skip, slots);
+                if (e == cudaSuccess && fn)
+                    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem_bytes(PKV_ATTN_MAX_SEQS, skip, slots)));
+            }
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) {
         record_cuda_error(e);
@@ -960,36 +982,56 @@ DeviceInfo device_info() {
     return d;
 }
 
-// Persistent CTAs for a batch of num_seqs: every CTA that fits at once (the
-// shared-memory prefix sum grows with num_seqs, so large batches may fit one
-// CTA per SM instead of two). 0 on error.
-int grid_for(int num_seqs, int block_tokens = PKV_BLOCK_TOKENS, bool skip = false) {
+// The launch shape for a batch of num_seqs: every CTA that fits at once (the
+// shared-memory prefix sum grows with num_seqs). Two merge slots while two
+// CTAs per SM still fit with them, else one when that keeps two per SM.
+struct KernelConfig {
+    int grid = 0;  // 0 on error
+    int slots = 2;
+    size_t smem = 0;
+    KernelFn fn = nullptr;
+};
+
+KernelConfig config_for(int num_seqs, int block_tokens = PKV_BLOCK_TOKENS, bool skip = false) {
     const DeviceInfo d = device_info();
-    const KernelFn fn = skip ? (block_tokens == PKV_BLOCK_TOKENS ? decode_kernel<PKV_BLOCK_TOKENS, true> : nullptr)
-                             : kernel_for(block_tokens);
-    if (!d.ok || !fn) return 0;
-    // Cached per (device, block size, shared memory size), so that a call
-    // made while a stream is being captured into a graph issues no CUDA query.
+    if (!d.ok || !kernel_for(block_tokens, skip, 2)) return {};
+    // Cached per (device, block size, skip, shared memory size), so that a
+    // call made while a stream is being captured into a graph issues no CUDA
+    // query.
     static std::mutex mu;
-    static std::map<std::pair<int, size_t>, int> cache;
+    static std::map<std::pair<int, size_t>, KernelConfig> cache;
     int dev = 0;
     cudaGetDevice(&dev);
-    const size_t smem = smem_bytes(num_seqs, skip);
-    const std::pair<int, size_t> key{(dev * 128 + block_tokens) * 2 + (skip ? 1 : 0), smem};
+    const std::pair<int, size_t> key{(dev * 128 + block_tokens) * 2 + (skip ? 1 : 0), smem_bytes(num_seqs, skip, 2)};
     {
         std::lock_guard<std::mutex> lock(mu);
         auto it = cache.find(key);
         if (it != cache.end()) return it->second;
     }
-    int per_sm = 0;
-    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, smem);
-    if (e != cudaSuccess || per_sm < 1) {
-        record_cuda_error(e);
-        return 0;
+    KernelConfig best;
+    for (int slots : {2, 1}) {
+        KernelConfig c;
+        c.slots = slots;
+        c.fn = kernel_for(block_tokens, skip, slots);
+        c.smem = smem_bytes(num_seqs, skip, slots);
+        int per_sm = 0;
+        const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, c.fn, kThreads, c.smem);
+        if (e != cudaSuccess) {
+            record_cuda_error(e);
+            return {};
+        }
+        c.grid = d.sm_count * per_sm;
+        if (c.grid > best.grid) best = c;
+        if (per_sm >= 2) break;
     }
+    if (best.grid < 1) return {};
     std::lock_guard<std::mutex> lock(mu);
-    cache[key] = d.sm_count * per_sm;
-    return d.sm_count * per_sm;
+    cache[key] = best;
+    return best;
+}
+
+int grid_for(int num_seqs, int block_tokens = PKV_BLOCK_TOKENS, bool skip = false) {
+    return config_for(num_seqs, block_tokens, skip).grid;
 }
 
 struct Launch {
@@ -1005,8 +1047,7 @@ pkv_status prepare(const void* q, const void* k_cache, const void* v_cache, cons
                    int max_blocks_per_seq, const int32_t* context_lens, int num_seqs, int num_q_heads,
                    int num_kv_heads, int head_dim, int num_blocks, float scale, int num_ctas, void* workspace,
                    size_t workspace_bytes, void* out, Launch* L, int block_tokens = PKV_BLOCK_TOKENS) {
-    L->fn = kernel_for(block_tokens);
-    if (!L->fn) return PKV_EUNSUPPORTED;
+    if (!kernel_for(block_tokens, false, 2)) return PKV_EUNSUPPORTED;
     if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !workspace || !out)
         return PKV_EINVAL;
     if (num_seqs < 1 || num_q_heads < 1 || num_kv_heads < 1 || num_blocks < 1 ||
@@ -1023,9 +1064,9 @@ pkv_status prepare(const void* q, const void* k_cache, const void* v_cache, cons
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
         (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
         return PKV_EINVAL;
-    const int auto_grid = grid_for(num_seqs, block_tokens);
-    if (auto_grid < 1) return PKV_ECUDA;
-    int grid = num_ctas > 0 ? num_ctas : auto_grid;
+    const KernelConfig kc = config_for(num_seqs, block_tokens);
+    if (kc.grid < 1) return PKV_ECUDA;
+    int grid = num_ctas > 0 ? num_ctas : kc.grid;
     const size_t fixed = kWsHeader + align256(static_cast<size_t>(num_seqs) * num_kv_heads * 4);
     if (workspace_bytes < fixed + 2 * kPartialFloats * 4) return PKV_EINVAL;
     const long long fit = static_cast<long long>((workspace_bytes - fixed) / (2 * kPartialFloats * 4));
@@ -1056,7 +1097,8 @@ pkv_status prepare(const void* q, const void* k_cache, const void* v_cache, cons
     prm.skip_tiles = nullptr;
     prm.side = nullptr;
     L->grid = grid;
-    L->smem = smem_bytes(num_seqs);
+    L->fn = kc.fn;
+    L->smem = kc.smem;
     return PKV_OK;
 }
 
@@ -1866,10 +1908,11 @@ pkv_status pkv_attn_decode_cascade(const void* q, const void* k_cache, const voi
     // the private pass: every sequence's tiles after its group's shared ones
     L.prm.skip_tiles = reinterpret_cast<const int32_t*>(ws + CL.skip_off);
     L.prm.side = reinterpret_cast<float*>(ws + CL.side_off);
-    L.fn = attn::decode_kernel<PKV_BLOCK_TOKENS, true>;
-    L.grid = std::min(L.grid, attn::grid_for(num_seqs, PKV_BLOCK_TOKENS, true));
-    L.smem = attn::smem_bytes(num_seqs, true);
-    if (L.grid < 1) return PKV_ECUDA;
+    const attn::KernelConfig kc = attn::config_for(num_seqs, PKV_BLOCK_TOKENS, true);
+    if (kc.grid < 1) return PKV_ECUDA;
+    L.fn = kc.fn;
+    L.grid = std::min(L.grid, kc.grid);
+    L.smem = kc.smem;
     st = attn::launch(L, s, false);
     if (CL.num_items > 0 && !cuda_ok(cudaStreamWaitEvent(s, side.join, 0))) return PKV_ECUDA;  // join first
     if (st != PKV_OK || CL.num_targets == 0) return st;
@@ -1963,11 +2006,11 @@ extern "C" pkv_status pkv_attn_decode_static(const void* q, const void* k_cache,
         static_cast<long long>(num_kv_heads) * num_seqs * (max_blocks_per_seq + attn::kPieceCost) >= (1ll << 30))
         return PKV_ERANGE;
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return PKV_EINVAL;
-    const int auto_grid = attn::grid_for(num_seqs);
-    if (auto_grid < 1) return PKV_ECUDA;
+    const attn::KernelConfig kc = attn::config_for(num_seqs);
+    if (kc.grid < 1) return PKV_ECUDA;
     uint8_t* scratch = attn::static_scratch_address();
     if (!scratch) return PKV_ECUDA;
-    const int grid = auto_grid < attn::kStaticMaxCtas ? auto_grid : attn::kStaticMaxCtas;
+    const int grid = kc.grid < attn::kStaticMaxCtas ? kc.grid : attn::kStaticMaxCtas;
 
     CUtensorMap tm_k, tm_v;
     if (!attn::make_cache_map(&tm_k, k_cache, num_blocks, num_kv_heads, PKV_BLOCK_TOKENS) ||
@@ -2003,9 +2046,10 @@ extern "C" pkv_status pkv_attn_decode_static(const void* q, const void* k_cache,
     prm.skip_tiles = nullptr;
     prm.side = nullptr;
 
-    attn::decode_kernel<PKV_BLOCK_TOKENS>
-        <<<grid, attn::kThreads, attn::smem_bytes(num_seqs), as_stream(stream)>>>(tm_k, tm_v, prm);
-    e = cudaGetLastError();
+    void* args[] = {&tm_k, &tm_v, &prm};
+    e = cudaLaunchKernel(reinterpret_cast<const void*>(kc.fn), dim3(grid), dim3(attn::kThreads), args, kc.smem,
+                         as_stream(stream));
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) {
         record_cuda_error(e);
         return PKV_ECUDA;

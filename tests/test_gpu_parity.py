@@ -192,6 +192,32 @@ def test_zero_and_clamped_contexts_and_bad_ids(pkv):
     _close(out[:3], ref[:3], None)
 
 
+def test_many_empty_contexts_between_short_and_long(pkv):
+    """Half the batch has no context, interleaved with 1..300-token and
+    900-token sequences: the work partition leaves cost gaps that hold no
+    tile, so some CTAs get no work and others start or end inside a gap."""
+    rng = np.random.default_rng(11)
+    B, Hq, Hkv, D, W = 40, 16, 2, 128, 64
+    NB = 400
+    kp, vp = randn_bf16(rng, (NB, Hkv, 16, D)), randn_bf16(rng, (NB, Hkv, 16, D))
+    q = randn_bf16(rng, (B, Hq, D))
+    tables = rng.integers(0, NB, size=(B, W)).astype(np.int32)
+    ctx = np.where(np.arange(B) % 2 == 0, 0, rng.integers(1, 301, size=B)).astype(np.int32)
+    ctx[[5, 17, 33]] = 900
+    ref = pa.paged_decode_attention(q, kp, vp, tables, ctx, 0.088)
+    dev = "cuda"
+    kc, vc = pkv.bf16_from_bits(kp).to(dev), pkv.bf16_from_bits(vp).to(dev)
+    qd = pkv.bf16_from_bits(q).to(dev)
+    td, cd = torch.from_numpy(tables).to(dev), torch.from_numpy(ctx).to(dev)
+    ws = pkv.AttentionWorkspace(B, Hkv)
+    for n in (0, 1, 2, 3, 9, 64, 151, 300):
+        out = pkv.attn_decode(qd, kc, vc, td, cd, 0.088, workspace=ws, num_ctas=n)
+        torch.cuda.synchronize()
+        assert ws.read_error() == 0
+        assert not out[0::2].any()
+        _close(out, ref)
+
+
 def test_append_and_copy_bit_exact_with_padding_and_bad_slots(pkv):
     rng = np.random.default_rng(6)
     NB, Hkv, D = 24, 8, 128

@@ -284,6 +284,16 @@ def many_short(seed: int = 0) -> Workload:
     return _decode_batch("many_short", "batch 4096, ctx U[1, 40], 32 q / 8 kv heads", seed, 32, 8, ctx)
 
 
+def large_batch(seed: int = 0, batch: int = 4096) -> Workload:
+    """A large decode batch at moderate contexts (lognormal, median 256 tokens,
+    clipped to [16, 2,048]): bandwidth-bound like the 64-sequence batch, but
+    with thousands of (sequence, KV head) runs per launch."""
+    r = _rng(seed, _TAG_PARAMS, 0)
+    ctx = _lognormal_lengths(r, batch, 256, 0.5, 16, 2048)
+    return _decode_batch(f"large_batch_{batch}", f"batch {batch}, lognormal(256, 0.5) ctx in [16, 2048], 32 q / 8 kv heads",
+                         seed, 32, 8, ctx)
+
+
 WORKLOADS = {
     "heads_8_8": lambda seed=0: heads(seed, 8, 8),
     "heads_16_8": lambda seed=0: heads(seed, 16, 8),
@@ -291,6 +301,8 @@ WORKLOADS = {
     "heads_64_8": lambda seed=0: heads(seed, 64, 8),
     "long_single": long_single,
     "many_short": many_short,
+    "large_batch_4096": lambda seed=0: large_batch(seed, 4096),
+    "large_batch_2048": lambda seed=0: large_batch(seed, 2048),
     "tiny": tiny,
     "tiny_nan": tiny_nan,
     "llama3_8b_b64": llama3_8b,
