@@ -132,7 +132,9 @@ pkv_status pkv_block_copy_ex(void* k_cache, void* v_cache, const int32_t* src_ds
  * pkv_attn_workspace_size -- bytes of device scratch pkv_attn_decode needs for
  * num_seqs sequences and num_kv_heads KV heads on the current device.
  * The workspace holds the error word (its first 4 bytes), one counter per
- * (sequence, KV head) and two fp32 partial results per CTA. Returns 0 for
+ * (sequence, KV head), and per CTA two fp32 partial results and two group
+ * counters (a pair split among more than eight CTAs merges in two levels).
+ * Returns 0 for
  * invalid arguments or when no device is present.
  */
 size_t pkv_attn_workspace_size(int num_seqs, int num_kv_heads);
@@ -331,7 +333,7 @@ int pkv_attn_default_ctas(int num_seqs);
  * Same computation, layouts and limits as pkv_attn_decode, plus:
  *  - num_seqs * num_kv_heads <= 16384 (else PKV_ERANGE); at most 512
  *    persistent CTAs;
- *  - the scratch (counters and fp32 partials, about 4.2 MiB) is one static
+ *  - the scratch (counters and fp32 partials, about 4.3 MiB) is one static
  *    device array inside this library; every GPU that loads the library holds
  *    it until the process exits. This call allocates and frees nothing: it
  *    clears the counters it uses with an asynchronous memset on `stream`,

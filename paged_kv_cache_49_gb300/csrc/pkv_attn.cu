@@ -75,6 +75,9 @@ constexpr int kQSlots = 2;
 // consumer warps, the merge warp's combine and any cross-CTA merge) costs a
 // CTA, next to streaming one 8 KB tile at its share of HBM bandwidth.
 constexpr int kPieceCost = 3;
+// Pairs split into more pieces than this merge in two levels (see the merge
+// warp).
+constexpr int kMergeGroup = 8;
 constexpr int kHalfBytes = kTok * 64 * 2;  // one 16 x 64 bf16 box
 constexpr int kBlockBytes = 2 * kHalfBytes;  // one K (or V) block of one KV head
 constexpr int kStageBytes = 2 * kBlockBytes;
@@ -122,9 +125,14 @@ constexpr size_t kWsHeader = 256;
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Per CTA: two partial slots and two group counters (two-level merges).
+constexpr size_t kWsPerCta = 2 * kPartialFloats * 4 + 2 * 4;
+
+// Workspace: header (error word), one counter per (sequence, KV head) pair,
+// then the CTAs' partial slots, then their group counters.
 inline size_t workspace_bytes(int num_seqs, int num_kv_heads, int grid) {
     return kWsHeader + align256(static_cast<size_t>(num_seqs) * num_kv_heads * 4) +
-           static_cast<size_t>(grid) * 2 * kPartialFloats * 4;
+           static_cast<size_t>(grid) * kWsPerCta;
 }
 
 struct Params {
@@ -143,6 +151,7 @@ struct Params {
     uint32_t* err;
     int* counters;
     float* partials;
+    int* group_counters;  // [grid][2]: pieces counted per group of a two-level merge
     // Cascade attention's private pass (both null otherwise): per sequence,
     // leading tiles to skip (computed elsewhere), and where a sequence with
     // skipped tiles leaves its unnormalised fp32 result instead of an output
@@ -645,39 +654,66 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             if (pieces > 1) {
                 // Publish this piece's partial (every lane's stores, ordered
                 // before lane 0's release by the warp barrier) and count it;
-                // the last piece of the pair to arrive acquires the others'.
-                __syncwarp();
-                int old = 0;
-                if (lane == 0) old = atom_add_acq_rel_gpu(p.counters + s * Hkv + g, 1);
-                old = __shfl_sync(0xffffffffu, old, 0);
-                __syncwarp();
-                if (old == pieces - 1) {  // last piece of the pair to finish: merge them all
-                    // An online log-sum-exp pass over the pieces, four pieces
-                    // (and four heads) at a time: each batch's loads are all
-                    // issued before any of them is used, so a pair split into
-                    // P pieces costs about P / 4 round trips to L2 (twice
-                    // that for groups of more than four heads), not P.
-                    float Mr[kMaxG], Lr[kMaxG];
-                    float4 Ar[kMaxG];
-#pragma unroll
-                    for (int h = 0; h < kMaxG; ++h) {
-                        Mr[h] = NEG_INF;
-                        Lr[h] = 0.f;
-                        Ar[h] = make_float4(0.f, 0.f, 0.f, 0.f);
+                // the last piece to arrive acquires the others' and merges.
+                // A pair of more than kMergeGroup pieces merges in two levels:
+                // the last arrival of each group of kMergeGroup consecutive
+                // pieces merges the group into the slot of its first piece,
+                // and the last group to finish merges the groups, so that no
+                // single warp walks dozens of partials at the kernel's end.
+                // group level: base = the group's first CTA, count = its
+                // pieces; pair level: base = i0, stride kMergeGroup (two
+                // levels) or 1, count = the groups or the pieces
+                bool group_level = pieces > kMergeGroup;
+                int base = i0, count = pieces;
+                if (group_level) {
+                    base = i0 + (static_cast<int>(blockIdx.x) - i0) / kMergeGroup * kMergeGroup;
+                    count = min(kMergeGroup, i1 - base + 1);
+                    if (count == 1) {  // a lone last piece is its group's result already
+                        base = i0;
+                        count = (pieces + kMergeGroup - 1) / kMergeGroup;
+                        group_level = false;
                     }
-                    for (int i = i0; i <= i1; i += 4) {
+                }
+                while (true) {
+                    const int stride = pieces > kMergeGroup && !group_level ? kMergeGroup : 1;
+                    int* ctr = group_level ? p.group_counters + 2 * base + (base == i1 ? 0 : 1)
+                                           : p.counters + s * Hkv + g;
+                    __syncwarp();
+                    int old = 0;
+                    if (lane == 0) old = atom_add_acq_rel_gpu(ctr, 1);
+                    old = __shfl_sync(0xffffffffu, old, 0);
+                    __syncwarp();
+                    if (old != count - 1) break;  // not the last arrival: done
+                    // An online log-sum-exp pass over the count partials at
+                    // CTAs base + n * stride, four heads at a time and four
+                    // partials per batch: each batch's loads are all issued
+                    // before any of them is used, so P partials cost about
+                    // P / 4 round trips to L2 per four heads, not P. A group's
+                    // result replaces its first piece's partial; the pair's
+                    // final result is emitted.
+                    float* gp = p.partials + (static_cast<size_t>(base) * 2 + (base == i1 ? 0 : 1)) * kPartialFloats;
 #pragma unroll
-                        for (int hb = 0; hb < kMaxG; hb += 4) {
-                            if (hb < G) {
+                    for (int hb = 0; hb < kMaxG; hb += 4) {
+                        if (hb < G) {
+                            float Mr[4], Lr[4];
+                            float4 Ar[4];
+#pragma unroll
+                            for (int h = 0; h < 4; ++h) {
+                                Mr[h] = NEG_INF;
+                                Lr[h] = 0.f;
+                                Ar[h] = make_float4(0.f, 0.f, 0.f, 0.f);
+                            }
+                            for (int n = 0; n < count; n += 4) {
                                 float mk[4][4], lk[4][4];
                                 float4 ok[4][4];
 #pragma unroll
                                 for (int k = 0; k < 4; ++k) {
+                                    const int cta = base + (n + k) * stride;
                                     const float* pi = p.partials +
-                                        (static_cast<size_t>(i + k) * 2 + (i + k == i1 ? 0 : 1)) * kPartialFloats;
+                                        (static_cast<size_t>(cta) * 2 + (cta == i1 ? 0 : 1)) * kPartialFloats;
 #pragma unroll
                                     for (int h = 0; h < 4; ++h) {
-                                        if (i + k <= i1 && hb + h < G) {
+                                        if (n + k < count && hb + h < G) {
                                             mk[k][h] = __ldcg(pi + (hb + h) * kORow + kDim);
                                             lk[k][h] = __ldcg(pi + (hb + h) * kORow + kDim + 1);
                                             ok[k][h] = __ldcg(reinterpret_cast<const float4*>(pi + (hb + h) * kORow + d0));
@@ -690,35 +726,50 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                                 }
 #pragma unroll
                                 for (int h = 0; h < 4; ++h) {
-                                    const int H = hb + h;
-                                    if (H < G) {
-                                        float mn = Mr[H];
+                                    float mn = Mr[h];
 #pragma unroll
-                                        for (int k = 0; k < 4; ++k) mn = fmaxf(mn, mk[k][h]);
-                                        const float a = ex2(Mr[H] - mn);
-                                        float L = Lr[H] * a;
-                                        float4 A = make_float4(Ar[H].x * a, Ar[H].y * a, Ar[H].z * a, Ar[H].w * a);
+                                    for (int k = 0; k < 4; ++k) mn = fmaxf(mn, mk[k][h]);
+                                    const float a = ex2(Mr[h] - mn);
+                                    float L = Lr[h] * a;
+                                    float4 A = make_float4(Ar[h].x * a, Ar[h].y * a, Ar[h].z * a, Ar[h].w * a);
 #pragma unroll
-                                        for (int k = 0; k < 4; ++k) {
-                                            const float b = ex2(mk[k][h] - mn);  // 0 for absent pieces
-                                            L += b * lk[k][h];
-                                            A.x += b * ok[k][h].x;
-                                            A.y += b * ok[k][h].y;
-                                            A.z += b * ok[k][h].z;
-                                            A.w += b * ok[k][h].w;
+                                    for (int k = 0; k < 4; ++k) {
+                                        const float b = ex2(mk[k][h] - mn);  // 0 for absent pieces
+                                        L += b * lk[k][h];
+                                        A.x += b * ok[k][h].x;
+                                        A.y += b * ok[k][h].y;
+                                        A.z += b * ok[k][h].z;
+                                        A.w += b * ok[k][h].w;
+                                    }
+                                    Mr[h] = mn;
+                                    Lr[h] = L;
+                                    Ar[h] = A;
+                                }
+                            }
+                            __syncwarp();  // every lane's loads of gp's rows precede lane 0's stores
+#pragma unroll
+                            for (int h = 0; h < 4; ++h) {
+                                const int H = hb + h;
+                                if (H < G) {
+                                    if (!group_level) {
+                                        emit(H, Ar[h], Mr[h], Lr[h]);
+                                    } else {
+                                        *reinterpret_cast<float4*>(gp + H * kORow + d0) = Ar[h];
+                                        if (lane == 0) {
+                                            gp[H * kORow + kDim] = Mr[h];
+                                            gp[H * kORow + kDim + 1] = Lr[h];
                                         }
-                                        Mr[H] = mn;
-                                        Lr[H] = L;
-                                        Ar[H] = A;
                                     }
                                 }
                             }
                         }
                     }
-#pragma unroll
-                    for (int h = 0; h < kMaxG; ++h)
-                        if (h < G) emit(h, Ar[h], Mr[h], Lr[h]);
-                    if (lane == 0) p.counters[s * Hkv + g] = 0;  // ready for the next launch
+                    if (lane == 0) *ctr = 0;  // ready for the next launch
+                    if (!group_level) break;
+                    // then count the group at the pair level
+                    base = i0;
+                    count = (pieces + kMergeGroup - 1) / kMergeGroup;
+                    group_level = false;
                 }
             }
             ++piece;
@@ -1068,8 +1119,8 @@ pkv_status prepare(const void* q, const void* k_cache, const void* v_cache, cons
     if (kc.grid < 1) return PKV_ECUDA;
     int grid = num_ctas > 0 ? num_ctas : kc.grid;
     const size_t fixed = kWsHeader + align256(static_cast<size_t>(num_seqs) * num_kv_heads * 4);
-    if (workspace_bytes < fixed + 2 * kPartialFloats * 4) return PKV_EINVAL;
-    const long long fit = static_cast<long long>((workspace_bytes - fixed) / (2 * kPartialFloats * 4));
+    if (workspace_bytes < fixed + kWsPerCta) return PKV_EINVAL;
+    const long long fit = static_cast<long long>((workspace_bytes - fixed) / kWsPerCta);
     if (grid > fit) {
         if (num_ctas > 0) return PKV_EINVAL;
         grid = static_cast<int>(fit);
@@ -1094,6 +1145,7 @@ pkv_status prepare(const void* q, const void* k_cache, const void* v_cache, cons
     prm.err = reinterpret_cast<uint32_t*>(ws);
     prm.counters = reinterpret_cast<int*>(ws + kWsHeader);
     prm.partials = reinterpret_cast<float*>(ws + fixed);
+    prm.group_counters = reinterpret_cast<int*>(ws + fixed + static_cast<size_t>(grid) * 2 * kPartialFloats * 4);
     prm.skip_tiles = nullptr;
     prm.side = nullptr;
     L->grid = grid;
@@ -1954,8 +2006,11 @@ namespace attn {
 constexpr int kStaticMaxCtas = 512;       // partial slots: 2 per CTA
 constexpr int kStaticMaxPairs = 16384;    // num_seqs * num_kv_heads counters
 constexpr size_t kStaticCounterBytes = static_cast<size_t>(kStaticMaxPairs) * 4;
-constexpr size_t kStaticScratchBytes =
-    kWsHeader + kStaticCounterBytes + static_cast<size_t>(kStaticMaxCtas) * 2 * kPartialFloats * 4;
+constexpr size_t kStaticGroupCounterBytes = static_cast<size_t>(kStaticMaxCtas) * 2 * 4;
+// header | group counters | pair counters | partial slots: the first three are
+// cleared by each call in one memset.
+constexpr size_t kStaticScratchBytes = kWsHeader + kStaticGroupCounterBytes + kStaticCounterBytes +
+                                       static_cast<size_t>(kStaticMaxCtas) * 2 * kPartialFloats * 4;
 
 static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
 
@@ -2020,7 +2075,8 @@ extern "C" pkv_status pkv_attn_decode_static(const void* q, const void* k_cache,
     // The counters must start at zero; a previous call leaves them at zero
     // unless it was cut short, so clear them (and the internal error word).
     cudaError_t e = cudaMemsetAsync(scratch, 0,
-                                    attn::kWsHeader + static_cast<size_t>(num_seqs) * num_kv_heads * 4,
+                                    attn::kWsHeader + attn::kStaticGroupCounterBytes +
+                                        static_cast<size_t>(num_seqs) * num_kv_heads * 4,
                                     as_stream(stream));
     if (e != cudaSuccess) {
         record_cuda_error(e);
@@ -2041,8 +2097,10 @@ extern "C" pkv_status pkv_attn_decode_static(const void* q, const void* k_cache,
     prm.num_blocks = num_blocks;
     prm.scale_log2 = scale * 1.4426950408889634f;
     prm.err = device_error ? device_error : reinterpret_cast<uint32_t*>(scratch);
-    prm.counters = reinterpret_cast<int*>(scratch + attn::kWsHeader);
-    prm.partials = reinterpret_cast<float*>(scratch + attn::kWsHeader + attn::kStaticCounterBytes);
+    prm.group_counters = reinterpret_cast<int*>(scratch + attn::kWsHeader);
+    prm.counters = reinterpret_cast<int*>(scratch + attn::kWsHeader + attn::kStaticGroupCounterBytes);
+    prm.partials = reinterpret_cast<float*>(scratch + attn::kWsHeader + attn::kStaticGroupCounterBytes +
+                                            attn::kStaticCounterBytes);
     prm.skip_tiles = nullptr;
     prm.side = nullptr;
 

@@ -87,9 +87,11 @@ def test_gqa_group_sizes(pkv, name):
 
 def test_long_single_sequence_merges_across_every_cta(pkv):
     """One 131,072-token sequence: each KV head's run is cut among ~38 CTAs,
-    so the last arrival merges dozens of partials."""
+    so its pieces merge in two levels (groups of eight, then the groups);
+    the grid sizes give 1-2, 8-9, 9-10, 16-17, 17-18 and 38-39 pieces per
+    pair (a lone last piece forms its own group)."""
     w = make_workload("long_single")
-    _run_workload(pkv, w, num_ctas_list=(0, 7))
+    _run_workload(pkv, w, num_ctas_list=(0, 7, 64, 72, 128, 136))
 
 
 def test_many_short_sequences_at_the_batch_limit(pkv):
