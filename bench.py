@@ -432,8 +432,10 @@ def run_ours(args):
         raise RuntimeError("device error word set during the timed steps")
 
     # ---- end to end through the C ABI's host-buffer step ----
-    # Every step: one copy of the packed inputs from pinned host memory, the
-    # step's kernels, one copy of the output rows back (pkv_decode_step_host).
+    # Every step (pkv_decode_step_host): the packed inputs brought from pinned
+    # host memory (a staging kernel reads them across the host link), the
+    # step's kernels, and the output rows written back to pinned host memory
+    # by the attention itself.
     e2e = None
     if not args.no_e2e:
         hs = pkv.HostStep(eng, B, sb.tables.shape[1], max_pairs=max(1, sb.num_pairs))

@@ -298,14 +298,16 @@ pkv_status pkv_step_layout(int num_seqs, int num_q_heads, int num_kv_heads, int 
 
 /*
  * pkv_decode_step_host -- pkv_decode_step with its inputs and output in host
- * memory: one copy of host_packed (laid out by pkv_step_layout; pinned
- * memory makes the copy asynchronous and fast) into device_staging (device,
- * layout.bytes, 256-byte aligned), the step itself reading its inputs from
- * there and writing attention rows to device_out (device, [num_seqs][Hq][D]
- * bf16), then one copy of those rows into host_out. When host_out is pinned
- * host memory the device can address (cudaHostAlloc / cudaHostRegister), the
- * attention writes the rows there directly and device_out is not touched
- * (it must still be a valid device pointer). Everything is enqueued
+ * memory: host_packed (laid out by pkv_step_layout) is brought into
+ * device_staging (device, layout.bytes, 256-byte aligned), the step itself
+ * reads its inputs from there and writes attention rows to device_out
+ * (device, [num_seqs][Hq][D] bf16), then one copy of those rows goes into
+ * host_out. When host_packed is pinned host memory the device can address
+ * (cudaHostAlloc / cudaHostRegister) and 16-byte aligned, a staging kernel
+ * reads it across the host link (faster than a copy engine for a step's
+ * ~1 MB); otherwise one asynchronous copy brings it. When host_out is such
+ * memory, the attention writes the rows there directly and device_out is not
+ * touched (it must still be a valid device pointer). Everything is enqueued
  * on `stream` and checked before anything is enqueued: host_packed must not
  * change, and host_out must not be read, until the stream has passed the
  * step (e.g. after cudaStreamSynchronize). This is the call through which a

@@ -333,8 +333,10 @@ def step_layout(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: in
 def decode_step_host(host_packed, device_staging, num_pairs, k_cache, v_cache, max_blocks_per_seq, num_seqs,
                      num_q_heads, scale, workspace, device_out, host_out, device_error=None, num_ctas: int = 0,
                      stream=None) -> None:
-    """pkv_decode_step_host: one H2D copy of the packed inputs (pinned uint8
-    host tensor), the step, one D2H copy of the output rows into host_out."""
+    """pkv_decode_step_host: the packed inputs (uint8 host tensor) staged into
+    device memory -- read across the host link by a kernel when pinned, else
+    one copy -- then the step, with the output rows written into host_out
+    (directly when pinned, else through device_out and one copy)."""
     _need(host_packed, torch.uint8, "host_packed", cuda=False)
     _need(device_staging, torch.uint8, "device_staging")
     _need(k_cache, torch.bfloat16, "k_cache")

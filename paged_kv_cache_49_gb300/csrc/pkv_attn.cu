@@ -1176,6 +1176,26 @@ pkv_status launch(const Launch& L, cudaStream_t stream, bool early) {
     return PKV_OK;
 }
 
+// Copy n16 16-byte words from pinned host memory that the device addresses
+// directly into device memory: every load crosses the host link at once, all
+// issued before any is stored (four per thread), where a copy engine takes
+// several times as long for the ~1 MB of a step's inputs.
+constexpr int kStageThreads = 256;
+constexpr int kStageUnroll = 4;
+
+__global__ void __launch_bounds__(kStageThreads) stage_kernel(const uint4* src, uint4* __restrict__ dst, size_t n16) {
+    const size_t stride = static_cast<size_t>(gridDim.x) * kStageThreads;
+    size_t i = static_cast<size_t>(blockIdx.x) * kStageThreads + threadIdx.x;
+    for (; i + (kStageUnroll - 1) * stride < n16; i += kStageUnroll * stride) {
+        uint4 v[kStageUnroll];
+#pragma unroll
+        for (int u = 0; u < kStageUnroll; ++u) v[u] = src[i + u * stride];
+#pragma unroll
+        for (int u = 0; u < kStageUnroll; ++u) dst[i + u * stride] = v[u];
+    }
+    for (; i < n16; i += stride) dst[i] = src[i];
+}
+
 }  // namespace attn
 }  // namespace pkv
 
@@ -1347,25 +1367,38 @@ pkv_status pkv_decode_step_host(const void* host_packed, void* device_staging, i
     const int32_t* pairs = num_pairs > 0 ? reinterpret_cast<const int32_t*>(d + lay.src_dst_pairs) : nullptr;
     const int32_t* tables = reinterpret_cast<const int32_t*>(d + lay.block_tables);
     const int32_t* ctx = reinterpret_cast<const int32_t*>(d + lay.context_lens);
-    // Output rows go straight to host_out when it is pinned host memory the
-    // device can address (the kernel's stores cross the host link as it
-    // finishes pieces), else to device_out and back in one copy.
-    void* direct = nullptr;
-    {
+    // Host buffers that are pinned memory the device can address are used in
+    // place: the inputs are staged by a kernel that reads them across the host
+    // link, and the output rows go straight to host_out (the attention's
+    // stores cross the link as it finishes pieces). Pageable buffers take a
+    // copy each way.
+    auto device_view = [](const void* h) -> void* {
         cudaPointerAttributes pa;
-        if (cudaPointerGetAttributes(&pa, host_out) == cudaSuccess) {
-            if (pa.type == cudaMemoryTypeHost && pa.devicePointer) direct = pa.devicePointer;
-        } else {
-            cudaGetLastError();  // pageable memory: not an error here
-        }
-    }
+        if (cudaPointerGetAttributes(&pa, h) == cudaSuccess)
+            return pa.type == cudaMemoryTypeHost ? pa.devicePointer : nullptr;
+        cudaGetLastError();  // pageable memory: not an error here
+        return nullptr;
+    };
+    void* direct = device_view(host_out);
+    const void* src = device_view(host_packed);
+    if (reinterpret_cast<uintptr_t>(src) & 15u) src = nullptr;
     attn::Launch L;
     st = check_step(k_new, v_new, slots, num_seqs, pairs, num_pairs, k_cache, v_cache, num_blocks, q, tables,
                     max_blocks_per_seq, ctx, num_seqs, num_q_heads, num_kv_heads, head_dim, scale, num_ctas,
                     workspace, workspace_bytes, direct ? direct : device_out, &L);
     if (st != PKV_OK) return st;
     cudaStream_t s = as_stream(stream);
-    cudaError_t e = cudaMemcpyAsync(device_staging, host_packed, lay.bytes, cudaMemcpyHostToDevice, s);
+    cudaError_t e = cudaSuccess;
+    if (src) {
+        const size_t n16 = lay.bytes / 16;  // lay.bytes is a multiple of 256
+        const size_t per_block = static_cast<size_t>(attn::kStageThreads) * attn::kStageUnroll;
+        const unsigned grid = static_cast<unsigned>(std::min<size_t>((n16 + per_block - 1) / per_block, 4096));
+        attn::stage_kernel<<<grid, attn::kStageThreads, 0, s>>>(static_cast<const uint4*>(src),
+                                                                static_cast<uint4*>(device_staging), n16);
+        e = cudaGetLastError();
+    } else {
+        e = cudaMemcpyAsync(device_staging, host_packed, lay.bytes, cudaMemcpyHostToDevice, s);
+    }
     if (e != cudaSuccess) {
         record_cuda_error(e);
         return PKV_ECUDA;

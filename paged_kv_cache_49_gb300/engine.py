@@ -224,8 +224,9 @@ class PagedKVEngine:
 class HostStep:
     """A decode step whose inputs and output live in host memory: one pinned
     packed input buffer (laid out by pkv_step_layout), its device staging
-    copy, and pinned output rows. run() is one pkv_decode_step_host call:
-    one host-to-device copy, the step's kernels, one device-to-host copy."""
+    buffer, and pinned output rows. run() is one pkv_decode_step_host call:
+    a staging kernel reads the inputs across the host link, the step's
+    kernels run, and the attention writes the output rows to host memory."""
 
     _DTYPES = {"q": torch.bfloat16, "k_new": torch.bfloat16, "v_new": torch.bfloat16, "slot_mapping": torch.int64,
                "block_tables": torch.int32, "context_lens": torch.int32, "src_dst_pairs": torch.int32}

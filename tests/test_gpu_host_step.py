@@ -1,5 +1,5 @@
-"""The host-buffer decode step (one packed host-to-device copy, the step,
-one device-to-host copy of the output) against the device-resident step:
+"""The host-buffer decode step (packed inputs staged from host memory, the
+step, output rows back in host memory) against the device-resident step:
 identical output rows and pools, bit for bit, and the oracle within
 tolerance."""
 import numpy as np
@@ -80,3 +80,35 @@ def test_host_step_output_to_pageable_memory(pkv):
                          w.num_q_heads, w.scale, step.workspace, step.out_dev, pageable, eng.error)
     torch.cuda.synchronize()
     assert torch.equal(pinned, pageable) and torch.equal(step.out_dev.cpu(), pageable)
+
+
+def test_host_step_inputs_from_pageable_memory(pkv):
+    """Pinned host_packed is staged by a kernel reading it across the host
+    link; pageable host_packed (and a pinned buffer at an offset that is not
+    16-byte aligned) go through one copy. All give the same rows and pools."""
+    w = make_workload("tiny")
+    q, k, v = w.step_inputs()
+    outs, pools = [], []
+    for mode in ("pinned", "pageable", "unaligned"):
+        eng = _engine(pkv, w)
+        slots, pairs = eng.bm.prepare_append(w.batch)
+        width = 16
+        tables, ctx = eng.bm.batch_tables(w.batch, width)
+        step = pkv.HostStep(eng, len(w.batch), width, max_pairs=4)
+        step.pack(pkv.bf16_from_bits(q), pkv.bf16_from_bits(k), pkv.bf16_from_bits(v), slots, tables, ctx, pairs)
+        packed = step.host
+        if mode == "pageable":
+            packed = step.host.clone()
+            assert not packed.is_pinned()
+        elif mode == "unaligned":
+            big = torch.empty(packed.numel() + 8, dtype=torch.uint8).pin_memory()
+            big[8:].copy_(packed)
+            packed = big[8:]
+        pkv.decode_step_host(packed, step.staging, step.num_pairs, eng.k_cache, eng.v_cache, width, len(w.batch),
+                             w.num_q_heads, w.scale, step.workspace, step.out_dev, step.out_host, eng.error)
+        torch.cuda.synchronize()
+        assert eng.read_errors() == 0 and step.workspace.read_error() == 0
+        outs.append(step.out_host.clone())
+        pools.append((eng.k_cache.clone(), eng.v_cache.clone()))
+    for o, (kc, vc) in zip(outs[1:], pools[1:]):
+        assert torch.equal(o, outs[0]) and torch.equal(kc, pools[0][0]) and torch.equal(vc, pools[0][1])
