@@ -556,6 +556,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             for (int w = 0; w < kConsumerWarps; ++w)
                 if (((w - gidx0 % kConsumerWarps) & (kConsumerWarps - 1)) < pc.len) owners |= 1u << w;
             gidx0 += pc.len;
+            if (nb == 1) continue;  // finished by its owner consumer warp
             // the CTAs holding pieces of this pair, from its cost positions
             const int seg_cost = Hkv * (scan[s] - nb) + g * nb + kPieceCost * (s * Hkv + g);
             const int i0 = seg_cost / cchunk;
@@ -911,6 +912,53 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             if (lane == 0) mbar_arrive(empty_bar(st));
         }
         gidx0 += len;
+
+        // ---- a pair of one tile: its owner warp finishes it alone ----
+        // Its state is the whole result (the merge warp's combine of a single
+        // warp's state gives the same numbers), so it skips the merge-slot
+        // hand-over, which for batches of short sequences is the chain every
+        // piece waits on; the merge warp skips such pieces too.
+        if (nb == 1) {
+            if (mine) {
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) {
+                    l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+                    l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+                }
+                const size_t row0 = static_cast<size_t>(s) * p.num_q_heads + static_cast<size_t>(pc.g) * G + 2 * c;
+                if (kSkip && skipped(s) > 0) {  // the cascade's unnormalised fp32 result
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        if (2 * c + h < G) {
+                            float* sd = p.side + (row0 + h) * kORow;
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                sd[16 * j + r] = o[j][h];
+                                sd[16 * j + r + 8] = o[j][h + 2];
+                            }
+                            if (r == 0) {
+                                sd[kDim] = h ? m1 : m0;
+                                sd[kDim + 1] = h ? l1 : l0;
+                            }
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        if (2 * c + h < G) {
+                            const float inv = 1.f / (h ? l1 : l0);
+                            __nv_bfloat16* dst = p.out + (row0 + h) * kDim;
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                dst[16 * j + r] = __float2bfloat16_rn(o[j][h] * inv);
+                                dst[16 * j + r + 8] = __float2bfloat16_rn(o[j][h + 2] * inv);
+                            }
+                        }
+                    }
+                }
+            }
+            continue;
+        }
 
         // ---- hand this warp's state for the piece to the merge warp ----
         // (a warp without blocks in the piece writes nothing: the merge warp
