@@ -1342,8 +1342,10 @@ pkv_status enqueue_step(const attn::Launch& L, const void* k_new, const void* v_
                              {static_cast<size_t>(p.num_seqs) * p.max_blocks * 4,
                               static_cast<size_t>(p.num_seqs) * p.num_q_heads * head_dim * 2,
                               static_cast<size_t>(p.num_seqs) * 4}};
+        // behind the step's block copies the append starts early and waits
+        // for them before its stores (it reads nothing they write)
         st = launch_append(k_new, v_new, slot_mapping, num_new_tokens, k_cache, v_cache, num_blocks, num_kv_heads,
-                           head_dim, PKV_BLOCK_TOKENS, device_error, stream, &warm);
+                           head_dim, PKV_BLOCK_TOKENS, device_error, stream, &warm, num_pairs > 0);
         if (st != PKV_OK) return st;
     }
     return attn::launch(L, as_stream(stream), num_pairs > 0 || num_new_tokens > 0);

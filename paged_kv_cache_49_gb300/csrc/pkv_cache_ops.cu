@@ -32,7 +32,9 @@ namespace ops {
 constexpr int kThreads = 256;
 
 // One thread per 16-byte vector of one (token, KV head) row of K or V.
-// vec_per_row = head_dim / 8.
+// vec_per_row = head_dim / 8. Launched early behind a step's block copy, it
+// loads its rows and slots while the copy runs and waits for the copy only
+// before its first store (a token may land in a block the copy fills).
 __global__ void __launch_bounds__(kThreads)
 append_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
               const int64_t* __restrict__ slots, long long rows, int hkv, int vec_per_row, int bt,
@@ -56,7 +58,9 @@ append_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
         const int vec = static_cast<int>(j - row * vec_per_row);
         const long long tok = row / hkv;
         const int head = static_cast<int>(row - tok * hkv);
+        const uint4 val = is_v ? __ldg(v + j) : __ldg(k + j);
         const long long slot = __ldg(slots + tok);
+        griddep_wait();  // the block copies this step launched before us are done
         if (slot < 0) continue;
         if (slot >= slot_limit) {
             if (err && vec == 0 && head == 0 && !is_v) atomicOr(err, PKV_DEVERR_SLOT);
@@ -65,8 +69,8 @@ append_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
         const long long blk = slot / bt;
         const long long pos = slot - blk * bt;
         const long long dst = ((blk * hkv + head) * bt + pos) * vec_per_row + vec;
-        if (is_v) v_cache[dst] = __ldg(v + j);
-        else k_cache[dst] = __ldg(k + j);
+        if (is_v) v_cache[dst] = val;
+        else k_cache[dst] = val;
     }
 }
 
@@ -148,7 +152,8 @@ static void prefer_shared_carveout() {
 
 pkv_status launch_append(const void* k, const void* v, const int64_t* slot_mapping, int num_tokens,
                          void* k_cache, void* v_cache, int num_blocks, int num_kv_heads, int head_dim,
-                         int block_tokens, uint32_t* device_error, void* stream, const L2Warm* warm) {
+                         int block_tokens, uint32_t* device_error, void* stream, const L2Warm* warm,
+                         bool early) {
     if (num_tokens < 0 || num_blocks < 1 || num_kv_heads < 1 || head_dim < 8 || head_dim % 8 != 0 ||
         block_tokens < 1)
         return PKV_EINVAL;
@@ -161,11 +166,24 @@ pkv_status launch_append(const void* k, const void* v, const int64_t* slot_mappi
     const long long work = 2 * rows * vec_per_row;
     const int grid = static_cast<int>(std::min<long long>((work + ops::kThreads - 1) / ops::kThreads, 65535));
     const L2Warm none = {{nullptr, nullptr, nullptr}, {0, 0, 0}};
-    ops::append_kernel<<<grid, ops::kThreads, 0, as_stream(stream)>>>(
-        static_cast<const uint4*>(k), static_cast<const uint4*>(v), slot_mapping, rows, num_kv_heads,
-        vec_per_row, block_tokens, static_cast<long long>(num_blocks) * block_tokens, static_cast<uint4*>(k_cache),
-        static_cast<uint4*>(v_cache), device_error, warm ? *warm : none);
-    const cudaError_t e = cudaGetLastError();
+    // early: programmatic stream serialization behind the step's block copy
+    // (whose kernel lets dependents start at once); the kernel waits for it
+    // before storing.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(ops::kThreads);
+    cfg.stream = as_stream(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = early ? 1 : 0;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, ops::append_kernel, static_cast<const uint4*>(k),
+                                       static_cast<const uint4*>(v), slot_mapping, rows, num_kv_heads, vec_per_row,
+                                       block_tokens, static_cast<long long>(num_blocks) * block_tokens,
+                                       static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), device_error,
+                                       warm ? *warm : none);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) {
         record_cuda_error(e);
         return PKV_ECUDA;
@@ -181,14 +199,14 @@ pkv_status pkv_append(const void* k, const void* v, const int64_t* slot_mapping,
                       void* k_cache, void* v_cache, int num_blocks, int num_kv_heads, int head_dim,
                       uint32_t* device_error, void* stream) {
     return launch_append(k, v, slot_mapping, num_tokens, k_cache, v_cache, num_blocks, num_kv_heads, head_dim,
-                         PKV_BLOCK_TOKENS, device_error, stream, nullptr);
+                         PKV_BLOCK_TOKENS, device_error, stream, nullptr, false);
 }
 
 pkv_status pkv_append_ex(const void* k, const void* v, const int64_t* slot_mapping, int num_tokens,
                          void* k_cache, void* v_cache, int num_blocks, int num_kv_heads, int head_dim,
                          int block_tokens, uint32_t* device_error, void* stream) {
     return launch_append(k, v, slot_mapping, num_tokens, k_cache, v_cache, num_blocks, num_kv_heads, head_dim,
-                         block_tokens, device_error, stream, nullptr);
+                         block_tokens, device_error, stream, nullptr, false);
 }
 
 pkv_status pkv_block_copy(void* k_cache, void* v_cache, const int32_t* src_dst_pairs, int num_pairs,

@@ -24,8 +24,13 @@ struct L2Warm {
 };
 
 // pkv_append's launch, optionally warming L2 with `warm` (may be null).
+// early: launched with programmatic stream serialization, allowed only right
+// behind a kernel of this library that writes none of the append's inputs
+// (the step's block copy): the kernel loads its rows first and waits for
+// that kernel before storing.
 pkv_status launch_append(const void* k, const void* v, const int64_t* slot_mapping, int num_tokens,
                          void* k_cache, void* v_cache, int num_blocks, int num_kv_heads, int head_dim,
-                         int block_tokens, uint32_t* device_error, void* stream, const L2Warm* warm);
+                         int block_tokens, uint32_t* device_error, void* stream, const L2Warm* warm,
+                         bool early);
 
 }  // namespace pkv
