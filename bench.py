@@ -37,7 +37,10 @@ sys.path.insert(0, ROOT)
 METRIC = "paged decode attention tokens/s and achieved HBM GB/s (% of GB300 peak)"
 UNIT = "tokens/s"
 L2_FLUSH_BYTES = 256 << 20
-KERNEL_SOURCE = os.path.join(ROOT, "paged_kv_cache_49_gb300", "csrc", "pkv_attn.cu")
+# The decode kernel's device code: a recorded ncu capture applies while these
+# are unchanged.
+KERNEL_SOURCES = [os.path.join(ROOT, "paged_kv_cache_49_gb300", "csrc", f)
+                  for f in ("pkv_decode_kernel.cuh", "pkv_ptx.cuh")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_dram_traffic.json")
 
 
@@ -117,8 +120,11 @@ def measured_peak_gbs():
 
 
 def kernel_hash():
-    with open(KERNEL_SOURCE, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    h = hashlib.sha256()
+    for path in KERNEL_SOURCES:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def recorded_traffic(workload, units):
