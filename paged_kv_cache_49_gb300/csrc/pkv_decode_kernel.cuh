@@ -455,6 +455,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             if (len >= kConsumerWarps) {  // short pieces: the consumers read their query rows themselves
                 if (lane == 0) {
                     if (mbar_wait(qempty_bar(qslot), qphase ^ 1u, abort_flag, p.err)) {
+                        fence_proxy_async_shared();  // the consumers' reads of the slot, before the copy over it
                         mbar_arrive_expect_tx(qfull_bar(qslot), G * kDim * 2);
                         const __nv_bfloat16* src =
                             p.q + (static_cast<size_t>(pc.s) * p.num_q_heads + static_cast<size_t>(pc.g) * G) * kDim;
@@ -819,6 +820,13 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 qb[2 * ks] = r < G ? *reinterpret_cast<const uint32_t*>(qs + ks * 32) : 0u;
                 qb[2 * ks + 1] = r < G ? *reinterpret_cast<const uint32_t*>(qs + ks * 32 + 16) : 0u;
             }
+            // The slot may be refilled as soon as it is released: every lane
+            // first holds its fragments (the loads have returned), else the
+            // producer's next bulk copy can land under loads still in flight.
+            uint32_t held = 0;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) held ^= qb[i];
+            wait_for_value(held);
             __syncwarp();
             if (lane == 0) mbar_arrive(qempty_bar(qslot));
             if (++qslot == kQSlots) { qslot = 0; qphase ^= 1u; }

@@ -28,6 +28,16 @@ __device__ __forceinline__ int atom_add_acq_rel_gpu(int* addr, int v) {
     return old;
 }
 
+// Orders this thread's earlier shared-memory accesses (generic proxy) before
+// its later bulk/TMA copies into shared memory (async proxy).
+__device__ __forceinline__ void fence_proxy_async_shared() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Holds the thread here until `v` is computed, i.e. until every load it
+// depends on has returned its data (a register use the scoreboard waits on).
+__device__ __forceinline__ void wait_for_value(uint32_t v) { asm volatile("" ::"r"(v) : "memory"); }
+
 // ---- mbarrier ----------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");

@@ -61,3 +61,45 @@ def test_static_scratch_entry_point_matches_workspace_entry_point():
         sb.tables.shape[1], sb.ctx.data_ptr(), 4096, hq, hkv, d, nb, ctypes.c_float(w.scale),
         None, out.data_ptr(), stream)
     assert too_many == nat.PKV_ERANGE
+
+
+def test_static_scratch_entry_point_at_a_large_batch():
+    """3,000 sequences: the one-merge-slot launch, through the static scratch
+    and through a caller workspace."""
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from tests.conftest import build_native
+    build_native()
+    import paged_kv_cache_49_gb300 as pkv
+    from paged_kv_cache_49_gb300 import _native as nat
+    from workloads import randn_bf16
+
+    rng = np.random.default_rng(3)
+    B, hq, hkv, d, bt = 3000, 16, 2, 128, 16
+    ctx = rng.integers(1, 90, size=B).astype(np.int32)
+    nblk = -(-ctx // bt)
+    width = int(nblk.max())
+    nb = int(nblk.sum()) + 4
+    perm = rng.permutation(nb).astype(np.int32)
+    tables = np.full((B, width), -1, np.int32)
+    nxt = 0
+    for s in range(B):
+        tables[s, :nblk[s]] = perm[nxt:nxt + nblk[s]]
+        nxt += int(nblk[s])
+    dev = torch.device("cuda")
+    t = lambda bits: pkv.bf16_from_bits(bits).to(dev)
+    kc, vc = t(randn_bf16(rng, (nb, hkv, bt, d))), t(randn_bf16(rng, (nb, hkv, bt, d)))
+    q = t(randn_bf16(rng, (B, hq, d)))
+    td, cd = torch.from_numpy(tables).to(dev), torch.from_numpy(ctx).to(dev)
+    scale = d ** -0.5
+    ref = pkv.attn_decode(q, kc, vc, td, cd, scale)
+    err = pkv.new_error_word()
+    out = torch.full_like(q, float("nan"))
+    status = nat.lib.pkv_attn_decode_static(
+        q.data_ptr(), kc.data_ptr(), vc.data_ptr(), td.data_ptr(), width, cd.data_ptr(), B, hq, hkv, d, nb,
+        ctypes.c_float(scale), err.data_ptr(), out.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert status == nat.PKV_OK
+    torch.cuda.synchronize()
+    assert pkv.read_device_error(err) == 0
+    diff = (out.float() - ref.float()).abs()
+    assert torch.isfinite(out.float()).all()
+    assert diff.max().item() <= MAX_ABS and diff.mean().item() <= MEAN_ABS
