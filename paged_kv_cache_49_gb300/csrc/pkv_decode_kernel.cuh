@@ -821,14 +821,15 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 qb[2 * ks + 1] = r < G ? *reinterpret_cast<const uint32_t*>(qs + ks * 32 + 16) : 0u;
             }
             // The slot may be refilled as soon as it is released: every lane
-            // first holds its fragments (the loads have returned), else the
-            // producer's next bulk copy can land under loads still in flight.
+            // first holds its fragments (the release below waits on a value
+            // computed from all of them, so on every load having returned),
+            // else the producer's next bulk copy can land under loads still
+            // in flight.
             uint32_t held = 0;
 #pragma unroll
             for (int i = 0; i < 16; ++i) held ^= qb[i];
-            wait_for_value(held);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(qempty_bar(qslot));
+            const uint32_t z = __reduce_or_sync(0xffffffffu, zero_after(held));  // 0, once all lanes hold theirs
+            if (lane == 0) mbar_arrive(qempty_bar(qslot) + z);
             if (++qslot == kQSlots) { qslot = 0; qphase ^= 1u; }
         } else if (mine) {
             const uint32_t* qg = reinterpret_cast<const uint32_t*>(

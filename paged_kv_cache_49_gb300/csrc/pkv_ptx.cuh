@@ -34,9 +34,14 @@ __device__ __forceinline__ void fence_proxy_async_shared() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// Holds the thread here until `v` is computed, i.e. until every load it
-// depends on has returned its data (a register use the scoreboard waits on).
-__device__ __forceinline__ void wait_for_value(uint32_t v) { asm volatile("" ::"r"(v) : "memory"); }
+// Zero, computed from `v` in a way no compiler pass can see through: adding
+// it to an address makes an instruction wait until `v` -- and every load `v`
+// was computed from -- is ready.
+__device__ __forceinline__ uint32_t zero_after(uint32_t v) {
+    uint32_t z;
+    asm volatile("and.b32 %0, %1, 0;" : "=r"(z) : "r"(v));
+    return z;
+}
 
 // ---- mbarrier ----------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
