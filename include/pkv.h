@@ -64,6 +64,7 @@ typedef int pkv_status;
 #define PKV_ATTN_HEAD_DIM 128   /* head_dim of pkv_attn_decode */
 #define PKV_ATTN_MAX_GROUP 8    /* max num_q_heads / num_kv_heads */
 #define PKV_ATTN_MAX_SEQS 4096  /* max num_seqs of one pkv_attn_decode call */
+#define PKV_ATTN_MAX_CTAS 2048  /* max num_ctas of one pkv_attn_decode call */
 
 /* Library version (major * 10000 + minor * 100 + patch). */
 int pkv_version(void);
@@ -130,12 +131,14 @@ pkv_status pkv_block_copy_ex(void* k_cache, void* v_cache, const int32_t* src_ds
 
 /*
  * pkv_attn_workspace_size -- bytes of device scratch pkv_attn_decode needs for
- * num_seqs sequences and num_kv_heads KV heads on the current device.
- * The workspace holds the error word (its first 4 bytes), one counter per
- * (sequence, KV head), and per CTA two fp32 partial results and two group
- * counters (a pair split among more than eight CTAs merges in two levels).
- * Returns 0 for
- * invalid arguments or when no device is present.
+ * num_seqs sequences and num_kv_heads KV heads on the current device (with
+ * the default num_ctas). The workspace holds the error word (its first 4
+ * bytes), a fixed 24 KiB of counters (three per possible CTA: one for a pair
+ * split across CTAs, two for the groups of a pair split among more than
+ * eight CTAs, which merges in two levels), then two fp32 partial results per
+ * CTA. The counters' place and size do not depend on the call, so one
+ * workspace serves calls of any batch, KV-head count and num_ctas that fit
+ * in it. Returns 0 for invalid arguments or when no device is present.
  */
 size_t pkv_attn_workspace_size(int num_seqs, int num_kv_heads);
 
@@ -159,10 +162,12 @@ pkv_status pkv_attn_workspace_init(void* workspace, size_t workspace_bytes, void
  *   q, out        : device bf16 [num_seqs][num_q_heads][128]
  *   block_tables  : device int32 [num_seqs][max_blocks_per_seq]
  *   context_lens  : device int32 [num_seqs]
- *   num_ctas      : number of persistent CTAs, 0 = as many as fit at once on
- *                   the device; the context of all (sequence, KV head) pairs
- *                   is split evenly among them and partial results of a pair
- *                   split across CTAs are merged in the same launch
+ *   num_ctas      : number of persistent CTAs (at most PKV_ATTN_MAX_CTAS, and
+ *                   as many as the workspace holds partial slots for), 0 =
+ *                   as many as fit at once on the device; the context of all
+ *                   (sequence, KV head) pairs is split evenly among them and
+ *                   partial results of a pair split across CTAs are merged in
+ *                   the same launch
  *   workspace     : device scratch of at least
  *                   pkv_attn_workspace_size(num_seqs, num_kv_heads) bytes,
  *                   zeroed once by pkv_attn_workspace_init; its first 4 bytes
@@ -184,6 +189,45 @@ pkv_status pkv_attn_decode(const void* q, const void* k_cache, const void* v_cac
                            int num_kv_heads, int head_dim, int num_blocks, float scale,
                            int num_ctas, void* workspace, size_t workspace_bytes,
                            void* out, void* stream);
+
+/*
+ * pkv_attn_decode_cuda_cores -- pkv_attn_decode with the per-tile math (the
+ * dot products of the query heads with each key, and the probability-
+ * weighted sum of the values) on the FP32 CUDA cores instead of the tensor
+ * cores; everything else (work split, copies, online softmax, merges) is the
+ * same kernel. For measuring the tensor-core choice: cs2680 Lecture 10,
+ * §10.3, step three says paging leaves the arithmetic unchanged, so which
+ * unit runs it is this library's decision. Group sizes
+ * num_q_heads / num_kv_heads of 4 and 8 only (PKV_EUNSUPPORTED otherwise);
+ * arguments, layouts and limits as pkv_attn_decode. The probabilities stay in
+ * fp32 here (the tensor-core kernel rounds them to bf16 for the mma), so the
+ * two agree within the attention tolerance, not bit for bit.
+ */
+pkv_status pkv_attn_decode_cuda_cores(const void* q, const void* k_cache, const void* v_cache,
+                                      const int32_t* block_tables, int max_blocks_per_seq,
+                                      const int32_t* context_lens, int num_seqs, int num_q_heads,
+                                      int num_kv_heads, int head_dim, int num_blocks, float scale, int num_ctas,
+                                      void* workspace, size_t workspace_bytes, void* out, void* stream);
+
+/*
+ * pkv_attn_decode_wait_test -- pkv_attn_decode for tests of the bounded-wait
+ * path only; its output is invalid. CTA 0's producer issues the copies of its
+ * first stop_tiles (>= 0) tiles and then stops, as if they never came: the
+ * consumer waiting on the next tile gives up after the wait limit (1 s),
+ * ORs PKV_DEVERR_TIMEOUT into the workspace's error word and raises the CTA's
+ * abort flag; the CTA then runs to its end without waiting, after waiting
+ * (bounded) for every copy it did issue. Nothing faults or hangs: this is
+ * how a kernel of this library ends when a copy never completes (cs2680
+ * Lecture 10, §10.5: a serving engine refuses or preempts instead of
+ * crashing). Zero the workspace with pkv_attn_workspace_init before its next
+ * use. Other arguments as pkv_attn_decode.
+ */
+pkv_status pkv_attn_decode_wait_test(const void* q, const void* k_cache, const void* v_cache,
+                                     const int32_t* block_tables, int max_blocks_per_seq,
+                                     const int32_t* context_lens, int num_seqs, int num_q_heads,
+                                     int num_kv_heads, int head_dim, int num_blocks, float scale, int num_ctas,
+                                     void* workspace, size_t workspace_bytes, void* out, int stop_tiles,
+                                     void* stream);
 
 /*
  * pkv_attn_decode_ex -- pkv_attn_decode over a cache of block_tokens-token
@@ -332,14 +376,14 @@ int pkv_attn_default_ctas(int num_seqs);
  * allocator, or a latency-critical loop that must never call cudaMalloc or
  * cudaFree). The pages describe no such variant: it has no counterpart there.
  *
- * Same computation, layouts and limits as pkv_attn_decode, plus:
- *  - num_seqs * num_kv_heads <= 16384 (else PKV_ERANGE); at most 512
- *    persistent CTAs;
- *  - the scratch (counters and fp32 partials, about 4.3 MiB) is one static
- *    device array inside this library; every GPU that loads the library holds
- *    it until the process exits. This call allocates and frees nothing: it
- *    clears the counters it uses with an asynchronous memset on `stream`,
- *    then launches the kernel;
+ * Same computation, layouts and limits as pkv_attn_decode (num_seqs above
+ * PKV_ATTN_MAX_SEQS is refused with PKV_EUNSUPPORTED), plus:
+ *  - at most 512 persistent CTAs (the default grid, capped);
+ *  - the scratch (counters and fp32 partials, 4,331,776 bytes, about 4.1 MiB)
+ *    is one static device array inside this library; every GPU that loads
+ *    the library holds it until the process exits. This call allocates and
+ *    frees nothing: it clears the counters with an asynchronous memset on
+ *    `stream`, then launches the kernel;
  *  - the first call on a device looks up that array's device address (a
  *    one-time set-up per device, with the device current); make that first
  *    call before any stream capture;

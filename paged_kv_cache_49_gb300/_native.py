@@ -31,6 +31,7 @@ BLOCK_TOKENS = 16
 HEAD_DIM = 128
 MAX_GROUP = 8
 MAX_SEQS = 4096
+MAX_CTAS = 2048
 
 EXPORTED = [
     "pkv_version", "pkv_status_string", "pkv_last_cuda_error", "pkv_read_device_error",
@@ -42,6 +43,7 @@ EXPORTED = [
     "pkv_block_copy_ex", "pkv_bm_create_ex", "pkv_bm_admit_tokens", "pkv_bm_preempt", "pkv_bm_resume",
     "pkv_bm_newest_running", "pkv_bm_slots", "pkv_step_layout", "pkv_decode_step_host",
     "pkv_attn_cascade_workspace_size", "pkv_cascade_staging_size", "pkv_cascade_plan", "pkv_attn_decode_cascade",
+    "pkv_attn_decode_wait_test", "pkv_attn_decode_cuda_cores",
 ]
 BLOCK_SIZES = (8, 16, 32, 64)
 
@@ -102,6 +104,10 @@ def _load() -> ctypes.CDLL:
         "pkv_attn_workspace_init": (i32, [vp, sz, vp]),
         "pkv_attn_decode": (i32, [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, f32, i32, vp, sz, vp, vp]),
         "pkv_attn_default_ctas": (i32, [i32]),
+        "pkv_attn_decode_cuda_cores": (i32, [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, f32, i32, vp, sz, vp,
+                                             vp]),
+        "pkv_attn_decode_wait_test": (i32, [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, f32, i32, vp, sz, vp,
+                                            i32, vp]),
         "pkv_attn_decode_static": (i32, [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, f32, vp, vp, vp]),
         "pkv_decode_step": (i32, [vp, vp, vp, i32, vp, i32, vp, vp, i32, vp, vp, i32, vp, i32, i32, i32, i32,
                                   f32, i32, vp, sz, vp, vp, vp]),
@@ -235,8 +241,9 @@ def default_ctas(num_seqs: int) -> int:
 
 
 class AttentionWorkspace:
-    """Device scratch for attn_decode: error word, per-(seq, KV head) counters
-    and per-CTA partials, zeroed once at creation."""
+    """Device scratch for attn_decode: error word, merge counters and per-CTA
+    partials, zeroed once at creation. One workspace serves calls of any
+    batch and grid whose partial slots fit in it."""
 
     def __init__(self, num_seqs: int, num_kv_heads: int, device=None, stream=None):
         nbytes = int(_lib.pkv_attn_workspace_size(num_seqs, num_kv_heads))
@@ -290,6 +297,35 @@ def attn_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out=None
                                      float(scale), int(num_ctas), workspace.ptr, workspace.nbytes,
                                      _ptr(out), _stream(stream))
     _check(st, "pkv_attn_decode")
+    return out
+
+
+def attn_decode_cuda_cores(q, k_cache, v_cache, block_tables, context_lens, scale, out=None, workspace=None,
+                           num_ctas: int = 0, stream=None):
+    """attn_decode with the per-tile math on the FP32 CUDA cores instead of
+    the tensor cores (group sizes 4 and 8, 16-token blocks): the measured
+    alternative to the tensor-core kernel."""
+    _need(q, torch.bfloat16, "q")
+    _need(k_cache, torch.bfloat16, "k_cache")
+    _need(v_cache, torch.bfloat16, "v_cache")
+    _need(block_tables, torch.int32, "block_tables")
+    _need(context_lens, torch.int32, "context_lens")
+    B, hq, d = q.shape
+    nb, hkv, bt, d2 = k_cache.shape
+    if d != d2 or v_cache.shape != k_cache.shape or bt != BLOCK_TOKENS:
+        raise ValueError("q [B, Hq, D] and caches [NB, Hkv, 16, D] must agree")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or context_lens.shape != (B,):
+        raise ValueError("block_tables must be [B, W] and context_lens [B]")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, torch.bfloat16, "out")
+    if workspace is None:
+        workspace = AttentionWorkspace(B, hkv, device=q.device, stream=stream)
+    _check(_lib.pkv_attn_decode_cuda_cores(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                           block_tables.shape[1], _ptr(context_lens), B, hq, hkv, d, nb,
+                                           float(scale), int(num_ctas), workspace.ptr, workspace.nbytes,
+                                           _ptr(out), _stream(stream)),
+           "pkv_attn_decode_cuda_cores")
     return out
 
 

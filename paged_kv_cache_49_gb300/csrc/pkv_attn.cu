@@ -75,6 +75,14 @@ KernelFn kernel_for(int block_tokens, bool skip, int slots) {
     return slots == 1 ? kernel_for_slots<1>(block_tokens, skip) : kernel_for_slots<2>(block_tokens, skip);
 }
 
+// The CUDA-core variant of the consumer math (16-token blocks), for group
+// sizes 4 and 8, else null.
+KernelFn kernel_fma_for(int slots, int group) {
+    if (group == 4) return slots == 1 ? decode_kernel<PKV_BLOCK_TOKENS, false, 1, 4> : decode_kernel<PKV_BLOCK_TOKENS, false, 2, 4>;
+    if (group == 8) return slots == 1 ? decode_kernel<PKV_BLOCK_TOKENS, false, 1, 8> : decode_kernel<PKV_BLOCK_TOKENS, false, 2, 8>;
+    return nullptr;
+}
+
 struct DeviceInfo {
     bool ok = false;
     int sm_count = 0;
@@ -99,6 +107,11 @@ DeviceInfo device_info() {
                     e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem_bytes(PKV_ATTN_MAX_SEQS, skip, slots)));
             }
+    for (int slots : {1, 2})
+        for (int group : {4, 8})
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(kernel_fma_for(slots, group), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem_bytes(PKV_ATTN_MAX_SEQS, false, slots)));
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) {
         record_cuda_error(e);
@@ -146,7 +159,7 @@ KernelConfig config_for(int num_seqs, int block_tokens = PKV_BLOCK_TOKENS, bool 
             record_cuda_error(e);
             return {};
         }
-        c.grid = d.sm_count * per_sm;
+        c.grid = std::min(d.sm_count * per_sm, kMaxCtas);
         if (c.grid > best.grid) best = c;
         if (per_sm >= 2) break;
     }
@@ -164,6 +177,7 @@ struct Launch {
     CUtensorMap tm_k, tm_v;
     Params prm;
     int grid;
+    int slots;
     size_t smem;
     KernelFn fn;
 };
@@ -177,7 +191,7 @@ pkv_status prepare(const void* q, const void* k_cache, const void* v_cache, cons
     if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !workspace || !out)
         return PKV_EINVAL;
     if (num_seqs < 1 || num_q_heads < 1 || num_kv_heads < 1 || num_blocks < 1 ||
-        max_blocks_per_seq < 1 || num_ctas < 0 || !std::isfinite(scale))
+        max_blocks_per_seq < 1 || num_ctas < 0 || num_ctas > kMaxCtas || !std::isfinite(scale))
         return PKV_EINVAL;
     if (num_seqs > PKV_ATTN_MAX_SEQS || head_dim != PKV_ATTN_HEAD_DIM ||
         num_q_heads % num_kv_heads != 0 || num_q_heads / num_kv_heads > PKV_ATTN_MAX_GROUP)
@@ -193,9 +207,8 @@ pkv_status prepare(const void* q, const void* k_cache, const void* v_cache, cons
     const KernelConfig kc = config_for(num_seqs, block_tokens);
     if (kc.grid < 1) return PKV_ECUDA;
     int grid = num_ctas > 0 ? num_ctas : kc.grid;
-    const size_t fixed = kWsHeader + align256(static_cast<size_t>(num_seqs) * num_kv_heads * 4);
-    if (workspace_bytes < fixed + kWsPerCta) return PKV_EINVAL;
-    const long long fit = static_cast<long long>((workspace_bytes - fixed) / kWsPerCta);
+    if (workspace_bytes < kWsFixed + kWsPerCta) return PKV_EINVAL;
+    const long long fit = static_cast<long long>((workspace_bytes - kWsFixed) / kWsPerCta);
     if (grid > fit) {
         if (num_ctas > 0) return PKV_EINVAL;
         grid = static_cast<int>(fit);
@@ -219,11 +232,13 @@ pkv_status prepare(const void* q, const void* k_cache, const void* v_cache, cons
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     prm.err = reinterpret_cast<uint32_t*>(ws);
     prm.counters = reinterpret_cast<int*>(ws + kWsHeader);
-    prm.partials = reinterpret_cast<float*>(ws + fixed);
-    prm.group_counters = reinterpret_cast<int*>(ws + fixed + static_cast<size_t>(grid) * 2 * kPartialFloats * 4);
+    prm.group_counters = prm.counters + kMaxCtas;
+    prm.partials = reinterpret_cast<float*>(ws + kWsFixed);
     prm.skip_tiles = nullptr;
     prm.side = nullptr;
+    prm.stop_tiles = -1;
     L->grid = grid;
+    L->slots = kc.slots;
     L->fn = kc.fn;
     L->smem = kc.smem;
     return PKV_OK;
@@ -287,7 +302,7 @@ size_t pkv_attn_workspace_size(int num_seqs, int num_kv_heads) {
     if (num_seqs <= 0 || num_kv_heads <= 0 || num_seqs > PKV_ATTN_MAX_SEQS) return 0;
     const int grid = attn::grid_for(num_seqs);
     if (grid < 1) return 0;
-    return attn::workspace_bytes(num_seqs, num_kv_heads, grid);
+    return attn::workspace_bytes(grid);
 }
 
 pkv_status pkv_attn_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
@@ -311,6 +326,48 @@ pkv_status pkv_attn_decode(const void* q, const void* k_cache, const void* v_cac
                                         num_seqs, num_q_heads, num_kv_heads, head_dim, num_blocks, scale,
                                         num_ctas, workspace, workspace_bytes, out, &L);
     if (st != PKV_OK) return st;
+    return attn::launch(L, as_stream(stream), false);
+}
+
+pkv_status pkv_attn_decode_cuda_cores(const void* q, const void* k_cache, const void* v_cache,
+                                      const int32_t* block_tables, int max_blocks_per_seq,
+                                      const int32_t* context_lens, int num_seqs, int num_q_heads,
+                                      int num_kv_heads, int head_dim, int num_blocks, float scale, int num_ctas,
+                                      void* workspace, size_t workspace_bytes, void* out, void* stream) {
+    attn::Launch L;
+    pkv_status st = attn::prepare(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                                  num_q_heads, num_kv_heads, head_dim, num_blocks, scale, num_ctas, workspace,
+                                  workspace_bytes, out, &L);
+    if (st != PKV_OK) return st;
+    const attn::KernelFn fn = attn::kernel_fma_for(L.slots, num_q_heads / num_kv_heads);
+    if (!fn) return PKV_EUNSUPPORTED;
+    if (num_ctas == 0) {  // every CTA of this instantiation that fits at once
+        const attn::DeviceInfo d = attn::device_info();
+        int per_sm = 0;
+        const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, attn::kThreads, L.smem);
+        if (e != cudaSuccess || per_sm < 1 || !d.ok) {
+            if (e != cudaSuccess) record_cuda_error(e);
+            return PKV_ECUDA;
+        }
+        L.grid = std::min(L.grid, d.sm_count * per_sm);
+    }
+    L.fn = fn;
+    return attn::launch(L, as_stream(stream), false);
+}
+
+pkv_status pkv_attn_decode_wait_test(const void* q, const void* k_cache, const void* v_cache,
+                                     const int32_t* block_tables, int max_blocks_per_seq,
+                                     const int32_t* context_lens, int num_seqs, int num_q_heads,
+                                     int num_kv_heads, int head_dim, int num_blocks, float scale, int num_ctas,
+                                     void* workspace, size_t workspace_bytes, void* out, int stop_tiles,
+                                     void* stream) {
+    if (stop_tiles < 0) return PKV_EINVAL;
+    attn::Launch L;
+    const pkv_status st = attn::prepare(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                                        num_seqs, num_q_heads, num_kv_heads, head_dim, num_blocks, scale,
+                                        num_ctas, workspace, workspace_bytes, out, &L);
+    if (st != PKV_OK) return st;
+    L.prm.stop_tiles = stop_tiles;
     return attn::launch(L, as_stream(stream), false);
 }
 
@@ -571,8 +628,12 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
 
     if (warp == kProducerWarp) {
         const uint64_t policy = policy_evict_first();
-        int stage = 0, issued = 0;
+        int stage = 0;
         uint32_t sphase = 0;
+        // stages that received a copy, and the phase parity of the last one
+        // (a stage is copied into only after its consumers saw its previous
+        // copy land, so that is the only copy that may be in flight)
+        uint32_t filled = 0, fill_par = 0;
         for (int it = blockIdx.x; it < p.num_items; it += gridDim.x) {
             const int4 item = p.items[it];
             const int g = item.z & 0xffff, n = item.z >> 16;
@@ -591,6 +652,7 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 for (int jj = 0; jj < cnt; ++jj) {
                     const int ya = __shfl_sync(0xffffffffu, y0, jj);
                     if (lane == 0 && mbar_wait(empty_bar(stage), sphase ^ 1u, abort_flag, p.err)) {
+                        fence_proxy_async_shared();  // the consumers' reads of the stage, before the copy over it
                         const uint32_t fb = full_bar(stage);
                         mbar_arrive_expect_tx(fb, kStageBytes);
                         const uint32_t dst = smem_u32(smem + stage * kStageBytes);
@@ -598,7 +660,8 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                         tma_load_2d(dst + kHalfBytes, &tm_k, 64, ya, fb, policy);
                         tma_load_2d(dst + kBlockBytes, &tm_v, 0, ya, fb, policy);
                         tma_load_2d(dst + kBlockBytes + kHalfBytes, &tm_v, 64, ya, fb, policy);
-                        ++issued;
+                        filled |= 1u << stage;
+                        fill_par = (fill_par & ~(1u << stage)) | (sphase << stage);
                     }
                     if (++stage == kPfxStages) { stage = 0; sphase ^= 1u; }
                 }
@@ -606,8 +669,8 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         }
         if (lane == 0) {  // no copy may land after the CTA exits (bounded waits)
             volatile int never = 0;
-            for (int i = max(0, issued - kPfxStages); i < issued; ++i)
-                mbar_wait(full_bar(i % kPfxStages), static_cast<uint32_t>((i / kPfxStages) & 1), &never, nullptr);
+            for (int i = 0; i < kPfxStages; ++i)
+                if ((filled >> i) & 1u) mbar_wait(full_bar(i), (fill_par >> i) & 1u, &never, nullptr);
         }
         return;
     }
@@ -645,7 +708,8 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         for (int j = 0; j < 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
         for (int t = 0; t < n; ++t, ++gi) {
             const int st = gi % kPfxStages;
-            mbar_wait(full_bar(st), static_cast<uint32_t>((gi / kPfxStages) & 1), abort_flag, p.err);
+            // released only once seen landed (an abort's early return must not free a stage in flight)
+            const bool landed = mbar_wait(full_bar(st), static_cast<uint32_t>((gi / kPfxStages) & 1), abort_flag, p.err);
             const uint32_t sk = smem_u32(smem + st * kStageBytes);
             const uint32_t sv = sk + kBlockBytes;
             float sa[4] = {0.f, 0.f, 0.f, 0.f};
@@ -692,7 +756,7 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 mma_bf16_16816(o[j], a, pb0, pb1);
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(empty_bar(st));
+            if (lane == 0 && landed) mbar_arrive(empty_bar(st));
         }
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
@@ -875,7 +939,7 @@ pkv_status cascade_layout(int num_seqs, int num_q_heads, int num_kv_heads, int n
     if (items > (1 << 28)) return PKV_ERANGE;
     const int grid = grid_for(num_seqs);
     if (grid < 1) return PKV_ECUDA;
-    L->decode_bytes = align256(workspace_bytes(num_seqs, num_kv_heads, grid));
+    L->decode_bytes = align256(workspace_bytes(grid));
     L->side_off = L->decode_bytes;
     L->skip_off = L->side_off + align256(static_cast<size_t>(num_seqs) * num_q_heads * kORow * 4);
     L->members_off = L->skip_off + align256(static_cast<size_t>(num_seqs) * 4);
@@ -1106,21 +1170,21 @@ pkv_status pkv_attn_decode_cascade(const void* q, const void* k_cache, const voi
 // plugin loaded into a host program that owns every device allocation and
 // gives plugins no allocator, or a latency-critical loop that must never pay
 // for cudaMalloc / cudaFree. Instead of a caller-provided workspace, the
-// partial results and per-(sequence, KV head) counters live in one
-// file-scope device array that every GPU loading this library holds until
-// the process exits.
+// partial results and the merge counters live in one file-scope device array
+// that every GPU loading this library holds until the process exits.
 
 namespace pkv {
 namespace attn {
 
-constexpr int kStaticMaxCtas = 512;       // partial slots: 2 per CTA
-constexpr int kStaticMaxPairs = 16384;    // num_seqs * num_kv_heads counters
-constexpr size_t kStaticCounterBytes = static_cast<size_t>(kStaticMaxPairs) * 4;
-constexpr size_t kStaticGroupCounterBytes = static_cast<size_t>(kStaticMaxCtas) * 2 * 4;
-// header | group counters | pair counters | partial slots: the first three are
+constexpr int kStaticMaxCtas = 512;  // partial slots: 2 per CTA
+// three counters per CTA: one per split pair (by its first CTA), two per
+// two-level merge group
+constexpr size_t kStaticCounterBytes = align256(static_cast<size_t>(kStaticMaxCtas) * 3 * 4);
+// header | counters | partial slots (4,331,776 bytes): the first two are
 // cleared by each call in one memset.
-constexpr size_t kStaticScratchBytes = kWsHeader + kStaticGroupCounterBytes + kStaticCounterBytes +
-                                       static_cast<size_t>(kStaticMaxCtas) * 2 * kPartialFloats * 4;
+constexpr size_t kStaticScratchBytes = kWsHeader + kStaticCounterBytes +
+                                       static_cast<size_t>(kStaticMaxCtas) * kWsPerCta;
+static_assert(kStaticScratchBytes == 4331776, "the static scratch size stated in pkv.h");
 
 static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
 
@@ -1164,7 +1228,6 @@ extern "C" pkv_status pkv_attn_decode_static(const void* q, const void* k_cache,
     if (num_seqs > PKV_ATTN_MAX_SEQS || head_dim != PKV_ATTN_HEAD_DIM || num_q_heads % num_kv_heads != 0 ||
         num_q_heads / num_kv_heads > PKV_ATTN_MAX_GROUP)
         return PKV_EUNSUPPORTED;
-    if (static_cast<long long>(num_seqs) * num_kv_heads > attn::kStaticMaxPairs) return PKV_ERANGE;
     if (static_cast<long long>(num_blocks) * num_kv_heads * PKV_BLOCK_TOKENS >= (1ll << 31) ||
         static_cast<long long>(num_seqs) * max_blocks_per_seq >= (1ll << 31) ||
         static_cast<long long>(max_blocks_per_seq) * PKV_BLOCK_TOKENS >= (1ll << 31) ||
@@ -1184,10 +1247,7 @@ extern "C" pkv_status pkv_attn_decode_static(const void* q, const void* k_cache,
 
     // The counters must start at zero; a previous call leaves them at zero
     // unless it was cut short, so clear them (and the internal error word).
-    cudaError_t e = cudaMemsetAsync(scratch, 0,
-                                    attn::kWsHeader + attn::kStaticGroupCounterBytes +
-                                        static_cast<size_t>(num_seqs) * num_kv_heads * 4,
-                                    as_stream(stream));
+    cudaError_t e = cudaMemsetAsync(scratch, 0, attn::kWsHeader + attn::kStaticCounterBytes, as_stream(stream));
     if (e != cudaSuccess) {
         record_cuda_error(e);
         return PKV_ECUDA;
@@ -1207,12 +1267,12 @@ extern "C" pkv_status pkv_attn_decode_static(const void* q, const void* k_cache,
     prm.num_blocks = num_blocks;
     prm.scale_log2 = scale * 1.4426950408889634f;
     prm.err = device_error ? device_error : reinterpret_cast<uint32_t*>(scratch);
-    prm.group_counters = reinterpret_cast<int*>(scratch + attn::kWsHeader);
-    prm.counters = reinterpret_cast<int*>(scratch + attn::kWsHeader + attn::kStaticGroupCounterBytes);
-    prm.partials = reinterpret_cast<float*>(scratch + attn::kWsHeader + attn::kStaticGroupCounterBytes +
-                                            attn::kStaticCounterBytes);
+    prm.counters = reinterpret_cast<int*>(scratch + attn::kWsHeader);
+    prm.group_counters = prm.counters + attn::kStaticMaxCtas;
+    prm.partials = reinterpret_cast<float*>(scratch + attn::kWsHeader + attn::kStaticCounterBytes);
     prm.skip_tiles = nullptr;
     prm.side = nullptr;
+    prm.stop_tiles = -1;
 
     void* args[] = {&tm_k, &tm_v, &prm};
     e = cudaLaunchKernel(reinterpret_cast<const void*>(kc.fn), dim3(grid), dim3(attn::kThreads), args, kc.smem,

@@ -50,6 +50,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <climits>
 #include <cstddef>
 #include <cstdint>
 
@@ -124,17 +125,28 @@ constexpr size_t smem_bytes(int num_seqs, bool skip, int slots) {
 
 constexpr size_t kWsHeader = 256;
 
-inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+__host__ __device__ constexpr size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Per CTA: two partial slots and two group counters (two-level merges).
-constexpr size_t kWsPerCta = 2 * kPartialFloats * 4 + 2 * 4;
+// Most persistent CTAs of one launch: the workspace keeps three counters for
+// each possible CTA (below), so that their place never depends on the launch.
+constexpr int kMaxCtas = PKV_ATTN_MAX_CTAS;
 
-// Workspace: header (error word), one counter per (sequence, KV head) pair,
-// then the CTAs' partial slots, then their group counters.
-inline size_t workspace_bytes(int num_seqs, int num_kv_heads, int grid) {
-    return kWsHeader + align256(static_cast<size_t>(num_seqs) * num_kv_heads * 4) +
-           static_cast<size_t>(grid) * kWsPerCta;
-}
+// Counters, per CTA c: [c] counts the pieces of the split pair whose first
+// piece is c's (a CTA's range ends inside at most one pair, so each split
+// pair has its own counter), [kMaxCtas + 2c + slot] counts the pieces of a
+// two-level merge group whose first piece is c's. Every launch leaves them at
+// zero. Their region has one size for every launch shape, so no launch ever
+// places a counter over memory that another launch (another batch or grid)
+// used for partials.
+constexpr size_t kWsCounterBytes = align256(static_cast<size_t>(kMaxCtas) * 3 * 4);
+
+// Per CTA: two fp32 partial slots.
+constexpr size_t kWsPerCta = 2 * kPartialFloats * 4;
+
+// Workspace: header (error word), the counters, then the CTAs' partial slots.
+constexpr size_t kWsFixed = kWsHeader + kWsCounterBytes;
+
+inline size_t workspace_bytes(int grid) { return kWsFixed + static_cast<size_t>(grid) * kWsPerCta; }
 
 struct Params {
     const __nv_bfloat16* q;
@@ -150,15 +162,19 @@ struct Params {
     int num_blocks;
     float scale_log2;
     uint32_t* err;
-    int* counters;
+    int* counters;        // [kMaxCtas]: pieces counted per split pair, by the pair's first CTA
     float* partials;
-    int* group_counters;  // [grid][2]: pieces counted per group of a two-level merge
+    int* group_counters;  // [kMaxCtas][2]: pieces counted per group of a two-level merge
     // Cascade attention's private pass (both null otherwise): per sequence,
     // leading tiles to skip (computed elsewhere), and where a sequence with
     // skipped tiles leaves its unnormalised fp32 result instead of an output
     // row ([num_seqs * num_q_heads][kORow]: output, max, sum).
     const int32_t* skip_tiles;
     float* side;
+    // Tests of the bounded-wait path only (-1 otherwise): CTA 0's producer
+    // issues the copies of its first stop_tiles tiles and skips the rest, so
+    // that a consumer's wait on the next one runs out.
+    int stop_tiles;
 };
 
 // Position in the line of (sequence, KV head) block runs.
@@ -281,13 +297,230 @@ struct PieceWalk {
     }
 };
 
+// ---- CUDA-core variant of the consumer math ----------------------------------
+// The same pieces, rings, online softmax and merge hand-off as the tensor-core
+// consumers, with the dot products and the P.V update on the FP32 pipe, so
+// that the choice of tensor cores for the GQA group tile can be measured
+// against it. G (the group size, 4 or 8) is a compile-time constant here.
+// Lane l owns head dims [4l, 4l + 4) of every query head of the group, for
+// K.q as for P.V: its q values (4 x G, pre-scaled into the log2 domain) stay
+// in registers. Per round of 32 / G tokens, each lane forms the partial dot
+// products of those tokens x G heads over its dims (32 values) and a
+// butterfly reduce-scatter over the warp (five exchange rounds) leaves lane L
+// with the whole score of token L / G, head L % G. The probabilities and the
+// per-head rescale factors reach every lane through the K half of the warp's
+// current stage, which is dead once the scores are formed.
+__device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int j = 0; j < o; ++j) {
+            const float keep = up ? v[o + j] : v[j];
+            const float send = up ? v[j] : v[o + j];
+            v[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+    return v[0];
+}
+
+template <int kSlots, int G>
+__device__ __forceinline__ void fma_consumer_warp(const Params& p, uint8_t* smem, const int* scan,
+                                                  const uint8_t* tail, int range_lo, int range_hi, int warp,
+                                                  int lane, volatile int* abort_flag, uint32_t bar0) {
+    static_assert(G == 4 || G == 8, "CUDA-core variant: group sizes 4 and 8");
+    using LY = Layout<kSlots>;
+    constexpr int kTpc = 32 / G;         // tokens per reduce-scatter round
+    constexpr int kRounds = kTok / kTpc; // rounds per tile
+    auto full_bar = [&](int i) { return bar0 + 8u * i; };
+    auto empty_bar = [&](int i) { return bar0 + 8u * (kStages + i); };
+    auto qfull_bar = [&](int i) { return bar0 + 8u * (2 * kStages + i); };
+    auto qempty_bar = [&](int i) { return bar0 + 8u * (2 * kStages + kQSlots + i); };
+    auto mfull_bar = [&](int i) { return bar0 + 8u * (2 * kStages + 2 * kQSlots + i); };
+    auto mempty_bar = [&](int i) { return bar0 + 8u * (2 * kStages + 2 * kQSlots + kSlots + i); };
+    float* sm_o = reinterpret_cast<float*>(smem + kOffO);
+    float* sm_m = reinterpret_cast<float*>(smem + LY::kOffM);
+    float* sm_l = reinterpret_cast<float*>(smem + LY::kOffL);
+    const int B = p.num_seqs, Hkv = p.num_kv_heads;
+    const int d0 = 4 * lane;
+    // dims [d0, d0 + 4) of a token row: box d0 / 64, 16-byte chunk (d0 % 64) / 8 (XOR-swizzled by the row), byte 0 or 8
+    const int box_off = (d0 >> 6) * kHalfBytes;
+    const int chunk = (d0 & 63) >> 3;
+    const int sub = (d0 & 7) * 2;
+    const int my_head = lane % G;
+    const int my_tok = lane / G;
+    const float NEG_INF = -INFINITY;
+
+    PieceWalk walk(scan, B, Hkv, range_lo, range_hi);
+    Piece pc;
+    int gidx0 = 0, qslot = 0, piece = 0;
+    uint32_t qphase = 0;
+    while (walk.next(pc)) {
+        const int s = pc.s, blk0 = pc.blk, nb = pc.nb, len = pc.len;
+        const int last_valid = tail[s];
+        const int first = (warp - static_cast<int>(gidx0 % kConsumerWarps)) & (kConsumerWarps - 1);
+        const bool mine = first < len;
+
+        float q[G][4];
+        auto take_q = [&](int h, uint2 w) {
+            q[h][0] = bf16_lo(w.x) * p.scale_log2;
+            q[h][1] = bf16_hi(w.x) * p.scale_log2;
+            q[h][2] = bf16_lo(w.y) * p.scale_log2;
+            q[h][3] = bf16_hi(w.y) * p.scale_log2;
+        };
+        if (len >= kConsumerWarps) {
+            const bool landed = mbar_wait(qfull_bar(qslot), qphase, abort_flag, p.err);
+            const uint8_t* qs = smem + kOffQ + qslot * kQBytes + d0 * 2;
+            uint32_t held = 0;
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const uint2 w = *reinterpret_cast<const uint2*>(qs + h * kDim * 2);
+                held ^= w.x ^ w.y;
+                take_q(h, w);
+            }
+            const uint32_t z = __reduce_or_sync(0xffffffffu, zero_after(held));  // 0, once all lanes hold theirs
+            if (lane == 0 && landed) mbar_arrive(qempty_bar(qslot) + z);
+            if (++qslot == kQSlots) { qslot = 0; qphase ^= 1u; }
+        } else if (mine) {
+            const __nv_bfloat16* qg = p.q + (static_cast<size_t>(s) * p.num_q_heads + static_cast<size_t>(pc.g) * G) * kDim + d0;
+#pragma unroll
+            for (int h = 0; h < G; ++h) take_q(h, __ldg(reinterpret_cast<const uint2*>(qg + h * kDim)));
+        }
+
+        float m_own = NEG_INF;  // running max of head my_head
+        float l_own = 0.f;      // this lane's share of head my_head's sum
+        float o[G][4];
+#pragma unroll
+        for (int h = 0; h < G; ++h) o[h][0] = o[h][1] = o[h][2] = o[h][3] = 0.f;
+
+        for (int jb = first; jb < len; jb += kConsumerWarps) {  // block gi goes to warp gi % 4, as in the tensor-core consumers
+            const int gi = gidx0 + jb;
+            const int st = static_cast<int>(gi % kStages);
+            const bool landed = mbar_wait(full_bar(st), static_cast<uint32_t>((gi / kStages) & 1), abort_flag, p.err);
+            const int valid = (blk0 + jb == nb - 1) ? last_valid : kTok;
+            uint8_t* stage = smem + kOffStages + st * kStageBytes;
+            const uint8_t* sk = stage + box_off;
+            const uint8_t* sv = stage + kBlockBytes + box_off;
+
+            float sc[kRounds];
+#pragma unroll
+            for (int c = 0; c < kRounds; ++c) {
+                float part[32];
+#pragma unroll
+                for (int tl = 0; tl < kTpc; ++tl) {
+                    const int t = c * kTpc + tl;
+                    const uint2 kw = *reinterpret_cast<const uint2*>(sk + t * 128 + (((chunk ^ (t & 7)) << 4) | sub));
+                    const float k0 = bf16_lo(kw.x), k1 = bf16_hi(kw.x), k2 = bf16_lo(kw.y), k3 = bf16_hi(kw.y);
+#pragma unroll
+                    for (int h = 0; h < G; ++h)
+                        part[tl * G + h] = fmaf(k3, q[h][3], fmaf(k2, q[h][2], fmaf(k1, q[h][1], k0 * q[h][0])));
+                }
+                sc[c] = reduce_scatter32(part, lane);  // token c * kTpc + my_tok, head my_head
+            }
+            float bm = NEG_INF;
+#pragma unroll
+            for (int c = 0; c < kRounds; ++c) {
+                if (c * kTpc + my_tok >= valid) sc[c] = NEG_INF;
+                bm = fmaxf(bm, sc[c]);
+            }
+#pragma unroll
+            for (int off = G; off < 32; off <<= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, off));
+            const float mn = fmaxf(m_own, bm);
+            const float al = ex2(m_own - mn);
+            m_own = mn;
+            // probabilities [16 tokens][G heads], then the G rescale factors,
+            // over the stage's first K box (every lane's K reads are done)
+            __syncwarp();
+            float* pb = reinterpret_cast<float*>(stage);
+            float lsum = 0.f;
+#pragma unroll
+            for (int c = 0; c < kRounds; ++c) {
+                const float pv = ex2(sc[c] - mn);
+                lsum += pv;
+                pb[c * 32 + lane] = pv;  // = pb[token * G + head]
+            }
+            l_own = l_own * al + lsum;
+            if (lane < G) pb[kTok * G + lane] = al;
+            __syncwarp();
+#pragma unroll
+            for (int h = 0; h < G; h += 4) {
+                const float4 a4 = *reinterpret_cast<const float4*>(pb + kTok * G + h);
+                const float a[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    o[h + u][0] *= a[u];
+                    o[h + u][1] *= a[u];
+                    o[h + u][2] *= a[u];
+                    o[h + u][3] *= a[u];
+                }
+            }
+#pragma unroll
+            for (int t = 0; t < kTok; ++t) {
+                uint2 vw = *reinterpret_cast<const uint2*>(sv + t * 128 + (((chunk ^ (t & 7)) << 4) | sub));
+                if (t >= valid) vw = make_uint2(0u, 0u);  // unwritten slots past the context never reach the output
+                const float v0 = bf16_lo(vw.x), v1 = bf16_hi(vw.x), v2 = bf16_lo(vw.y), v3 = bf16_hi(vw.y);
+#pragma unroll
+                for (int h = 0; h < G; h += 4) {
+                    const float4 p4 = *reinterpret_cast<const float4*>(pb + t * G + h);
+                    const float pr[4] = {p4.x, p4.y, p4.z, p4.w};
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        o[h + u][0] = fmaf(pr[u], v0, o[h + u][0]);
+                        o[h + u][1] = fmaf(pr[u], v1, o[h + u][1]);
+                        o[h + u][2] = fmaf(pr[u], v2, o[h + u][2]);
+                        o[h + u][3] = fmaf(pr[u], v3, o[h + u][3]);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0 && landed) mbar_arrive(empty_bar(st));
+        }
+        gidx0 += len;
+
+        if (mine) {  // the whole sum of head my_head in every lane of that head
+#pragma unroll
+            for (int off = G; off < 32; off <<= 1) l_own += __shfl_xor_sync(0xffffffffu, l_own, off);
+        }
+        if (nb == 1) {  // a pair of one tile: its owner warp writes the rows
+            if (mine) {
+                __nv_bfloat16* dst = p.out + (static_cast<size_t>(s) * p.num_q_heads + static_cast<size_t>(pc.g) * G) * kDim + d0;
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    const float inv = 1.f / __shfl_sync(0xffffffffu, l_own, h);
+                    uint2 w2;
+                    w2.x = pack_bf16x2(o[h][0] * inv, o[h][1] * inv);
+                    w2.y = pack_bf16x2(o[h][2] * inv, o[h][3] * inv);
+                    *reinterpret_cast<uint2*>(dst + h * kDim) = w2;
+                }
+            }
+            continue;
+        }
+        const int ms = piece % kSlots;
+        mbar_wait(mempty_bar(ms), static_cast<uint32_t>(((piece / kSlots) & 1) ^ 1), abort_flag, p.err);
+        if (mine) {
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+                *reinterpret_cast<float4*>(sm_o + ms * kMergeOFloats + (warp * kMaxG + h) * kORow + d0) =
+                    make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
+            if (lane < G) {
+                sm_m[ms * kMergeMLFloats + warp * kMaxG + lane] = m_own;
+                sm_l[ms * kMergeMLFloats + warp * kMaxG + lane] = l_own;
+            }
+        }
+        mbar_arrive(mfull_bar(ms));
+        ++piece;
+    }
+}
+
 // kBT: tokens per cache block (8, 16, 32 or 64). A 16-token tile is rows
 // [(t mod kBT/16) * 16, +16) of block table[t / (kBT/16)] when kBT >= 16, and
 // the two 8-row blocks table[2t], table[2t + 1] when kBT == 8.
 // kSkip: the private pass of cascade attention (per-sequence skipped tiles,
 // fp32 results for grouped sequences); a separate instantiation, so that the
 // plain kernel carries none of its branches. kSlots: merge slots (1 or 2).
-template <int kBT, bool kSkip, int kSlots>
+// kFmaG: 0 for the tensor-core consumers; 4 or 8 for the CUDA-core variant
+// of their math compiled for that group size (16-token blocks only).
+template <int kBT, bool kSkip, int kSlots, int kFmaG = 0>
 __global__ void __launch_bounds__(kThreads, 2)
 decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
               const Params p) {
@@ -447,8 +680,16 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         Piece pc;
         int stage = 0, qslot = 0;
         uint32_t sphase = 0, qphase = 0;
-        int issued = 0;
-        int q_issued = 0;
+        int tile = 0;  // position in the CTA's stream of tiles
+        const int stop_at = (p.stop_tiles >= 0 && blockIdx.x == 0) ? p.stop_tiles : INT_MAX;
+        // Lane 0's record of the copies it issued, for the drain before exit:
+        // bit i of `filled` = stage i received a copy, bit i of `fill_par` =
+        // the phase parity of its last one (q_filled / q_fill_par: the same
+        // for the query slots). A consumer releases a stage only after it saw
+        // the stage's copy land, and the producer copies into a stage only
+        // after its release, so every copy but the last into each stage has
+        // landed.
+        uint32_t filled = 0, fill_par = 0, q_filled = 0, q_fill_par = 0;
         bool waited = false;  // griddep_wait done by this thread
         while (walk.next(pc)) {
             const int len = pc.len;
@@ -460,7 +701,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                         const __nv_bfloat16* src =
                             p.q + (static_cast<size_t>(pc.s) * p.num_q_heads + static_cast<size_t>(pc.g) * G) * kDim;
                         bulk_load(smem_u32(smem + kOffQ + qslot * kQBytes), src, G * kDim * 2, qfull_bar(qslot));
-                        ++q_issued;
+                        q_filled |= 1u << qslot;
+                        q_fill_par = (q_fill_par & ~(1u << qslot)) | (qphase << qslot);
                     }
                 }
                 if (++qslot == kQSlots) { qslot = 0; qphase ^= 1u; }
@@ -498,7 +740,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                             griddep_wait();
                             waited = true;
                         }
-                        if (mbar_wait(empty_bar(stage), sphase ^ 1u, abort_flag, p.err)) {
+                        // (tests of the bounded waits: past stop_at nothing is issued)
+                        if (tile < stop_at && mbar_wait(empty_bar(stage), sphase ^ 1u, abort_flag, p.err)) {
+                            fence_proxy_async_shared();  // the consumer's reads of the stage, before the copy over it
                             const uint32_t fb = full_bar(stage);
                             mbar_arrive_expect_tx(fb, kStageBytes);
                             const uint32_t dst = smem_u32(smem + kOffStages + stage * kStageBytes);
@@ -518,25 +762,26 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                                 tma_load_2d(dst + kBlockBytes + kHalfBytes, &tm_v, 64, ya, fb, policy);
                                 tma_load_2d(dst + kBlockBytes + kHalfBytes + kRow8, &tm_v, 64, yb, fb, policy);
                             }
-                            ++issued;
+                            filled |= 1u << stage;
+                            fill_par = (fill_par & ~(1u << stage)) | (sphase << stage);
                         }
                     }
                     if (++stage == kStages) { stage = 0; sphase ^= 1u; }
+                    ++tile;
                 }
             }
         }
         // Before this warp exits, wait (bounded, even after an abort) for the
-        // copies it issued that may still be in flight, so that no TMA lands in
-        // shared memory after the CTA has exited. Copies were issued in order,
-        // so those are at most the last kStages blocks and kQSlots query loads.
+        // last copy into each stage and query slot, so that no copy lands in
+        // shared memory after the CTA has exited (every earlier copy has
+        // landed: see `filled`).
         if (!waited) griddep_wait();
         if (lane == 0) {
             volatile int never = 0;
-            for (int i = max(0, issued - kStages); i < issued; ++i)
-                mbar_wait(full_bar(static_cast<int>(i % kStages)),
-                          static_cast<uint32_t>((i / kStages) & 1), &never, nullptr);
-            for (int i = max(0, q_issued - kQSlots); i < q_issued; ++i)
-                mbar_wait(qfull_bar(i % kQSlots), static_cast<uint32_t>((i / kQSlots) & 1), &never, nullptr);
+            for (int i = 0; i < kStages; ++i)
+                if ((filled >> i) & 1u) mbar_wait(full_bar(i), (fill_par >> i) & 1u, &never, nullptr);
+            for (int i = 0; i < kQSlots; ++i)
+                if ((q_filled >> i) & 1u) mbar_wait(qfull_bar(i), (q_fill_par >> i) & 1u, &never, nullptr);
         }
         return;
     }
@@ -680,7 +925,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 while (true) {
                     const int stride = pieces > kMergeGroup && !group_level ? kMergeGroup : 1;
                     int* ctr = group_level ? p.group_counters + 2 * base + (base == i1 ? 0 : 1)
-                                           : p.counters + s * Hkv + g;
+                                           : p.counters + i0;
                     __syncwarp();
                     int old = 0;
                     if (lane == 0) old = atom_add_acq_rel_gpu(ctr, 1);
@@ -781,6 +1026,11 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     }
 
     // ========================= consumer warps =========================
+    if constexpr (kFmaG > 0) {
+        static_assert(kBT == kTok && !kSkip, "the CUDA-core variant serves the plain 16-token kernel");
+        fma_consumer_warp<kSlots, kFmaG>(p, smem, scan, tail, range_lo, range_hi, warp, lane, abort_flag, bar0);
+        return;
+    }
     const int r = lane >> 2;  // mma group id: token row / head column owner
     const int c = lane & 3;   // thread in group
     const uint32_t stage_base = smem_u32(smem + kOffStages);
@@ -813,7 +1063,11 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         // for a piece it takes no part in.
         uint32_t qb[16];
         if (len >= kConsumerWarps) {
-            mbar_wait(qfull_bar(qslot), qphase, abort_flag, p.err);
+            // A slot (or stage, below) is released only once this warp saw
+            // its copy land: after an abort a wait gives up early, and
+            // releasing then would let the producer copy into a slot whose
+            // previous copy is still in flight.
+            const bool landed = mbar_wait(qfull_bar(qslot), qphase, abort_flag, p.err);
             const uint8_t* qs = smem + kOffQ + qslot * kQBytes + r * (kDim * 2) + c * 4;
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
@@ -829,7 +1083,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
 #pragma unroll
             for (int i = 0; i < 16; ++i) held ^= qb[i];
             const uint32_t z = __reduce_or_sync(0xffffffffu, zero_after(held));  // 0, once all lanes hold theirs
-            if (lane == 0) mbar_arrive(qempty_bar(qslot) + z);
+            if (lane == 0 && landed) mbar_arrive(qempty_bar(qslot) + z);
             if (++qslot == kQSlots) { qslot = 0; qphase ^= 1u; }
         } else if (mine) {
             const uint32_t* qg = reinterpret_cast<const uint32_t*>(
@@ -855,7 +1109,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         for (int jb = first; jb < len; jb += kConsumerWarps) {
             const int gi = gidx0 + jb;
             const int st = static_cast<int>(gi % kStages);
-            mbar_wait(full_bar(st), static_cast<uint32_t>((gi / kStages) & 1), abort_flag, p.err);
+            const bool landed = mbar_wait(full_bar(st), static_cast<uint32_t>((gi / kStages) & 1), abort_flag, p.err);
             const int valid = (blk0 + jb == nb - 1) ? last_valid : kTok;
             const uint32_t sk = stage_base + st * kStageBytes;
             const uint32_t sv = sk + kBlockBytes;
@@ -919,7 +1173,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 mma_bf16_16816(o[j], a, pb0, pb1);
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(empty_bar(st));
+            if (lane == 0 && landed) mbar_arrive(empty_bar(st));
         }
         gidx0 += len;
 

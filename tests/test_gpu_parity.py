@@ -240,3 +240,46 @@ def test_append_and_copy_bit_exact_with_padding_and_bad_slots(pkv):
     assert pkv.read_device_error(err) == pkv.DEVERR_BLOCK_ID
     cache_ops.copy_blocks(k_ref, v_ref, pairs[:3])
     assert np.array_equal(pkv.bits_from_bf16(kc), k_ref) and np.array_equal(pkv.bits_from_bf16(vc), v_ref)
+
+
+def test_one_workspace_serves_any_launch_shape(pkv):
+    """One workspace, calls of different batches, KV-head counts and grids in
+    turn, with the bytes past the counters filled with garbage before each
+    call (what earlier launches leave in their partial slots): every call
+    must match the oracle. Pairs of 313 tiles are cut among up to ~100 CTAs,
+    so their merges run in two levels (group counters) as well as one."""
+    rng = np.random.default_rng(21)
+    D, dev = 128, "cuda"
+    # the workspace's counters: bytes [256, 256 + 2048 * 3 * 4) (a 256-byte
+    # header holds the error word); nothing after them has to start at zero
+    counters_end = 256 + ((pkv.MAX_CTAS * 3 * 4 + 255) // 256) * 256
+    shapes = []
+    for B, Hq, Hkv, ctx in ((3, 16, 2, [5000, 37, 1200]), (40, 32, 8, None), (1, 8, 1, [20000])):
+        if ctx is None:
+            ctx = rng.integers(1, 700, size=B).tolist()
+            ctx[7] = 4000
+        ctx = np.array(ctx, dtype=np.int32)
+        nblk = -(-ctx // 16)
+        NB = int(nblk.sum()) + 3
+        perm = rng.permutation(NB).astype(np.int32)
+        tables = np.full((B, int(nblk.max())), -1, np.int32)
+        nxt = 0
+        for s in range(B):
+            tables[s, :nblk[s]] = perm[nxt:nxt + nblk[s]]
+            nxt += int(nblk[s])
+        kp, vp = randn_bf16(rng, (NB, Hkv, 16, D)), randn_bf16(rng, (NB, Hkv, 16, D))
+        q = randn_bf16(rng, (B, Hq, D))
+        ref = pa.paged_decode_attention(q, kp, vp, tables, ctx, D ** -0.5)
+        shapes.append(dict(ref=ref, q=pkv.bf16_from_bits(q).to(dev), k=pkv.bf16_from_bits(kp).to(dev),
+                           v=pkv.bf16_from_bits(vp).to(dev), t=torch.from_numpy(tables).to(dev),
+                           c=torch.from_numpy(ctx).to(dev)))
+    ws = pkv.AttentionWorkspace(64, 8)
+    for i, (which, n) in enumerate([(0, 300), (0, 64), (1, 151), (0, 9), (2, 300), (1, 0), (2, 17), (0, 0)]):
+        sh = shapes[which]
+        ws.tensor[counters_end:].fill_(0x5B + i)
+        out = torch.full_like(sh["q"], float("nan"))
+        pkv.attn_decode(sh["q"], sh["k"], sh["v"], sh["t"], sh["c"], D ** -0.5, out, workspace=ws, num_ctas=n)
+        torch.cuda.synchronize()
+        assert ws.read_error() == 0
+        assert not ws.tensor[4:counters_end].any(), "counters left nonzero"
+        _close(out, sh["ref"])

@@ -55,12 +55,12 @@ def test_static_scratch_entry_point_matches_workspace_entry_point():
         assert torch.isfinite(out.float()).all()
         assert diff.max().item() <= MAX_ABS and diff.mean().item() <= MEAN_ABS
 
-    # sizes past the static limit are refused before any launch
+    # batches past the kernel's limit are refused before any launch
     too_many = nat.lib.pkv_attn_decode_static(
         sb.q.data_ptr(), eng.k_cache.data_ptr(), eng.v_cache.data_ptr(), sb.tables.data_ptr(),
-        sb.tables.shape[1], sb.ctx.data_ptr(), 4096, hq, hkv, d, nb, ctypes.c_float(w.scale),
+        sb.tables.shape[1], sb.ctx.data_ptr(), nat.MAX_SEQS + 1, hq, hkv, d, nb, ctypes.c_float(w.scale),
         None, out.data_ptr(), stream)
-    assert too_many == nat.PKV_ERANGE
+    assert too_many == nat.PKV_EUNSUPPORTED
 
 
 def test_static_scratch_entry_point_at_a_large_batch():
