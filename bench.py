@@ -3,19 +3,22 @@
 A step is the whole hot path for one batch: copy-on-write block copies (when
 the step has any), the append of each sequence's new token, and decode
 attention over every sequence's full context, for one attention layer.
-Default workload: Llama-3-8B geometry (32 q / 8 kv heads, d_h 128, bf16,
-16-token blocks), batch 64, lognormal(1024, 1.0) contexts clipped to
-[1, 8192], permuted pool with 10% free blocks.
+Default workload (the headline): Llama-3.3-70B geometry (64 q / 8 kv heads,
+d_h 128, bf16, 16-token blocks), batch 256, lognormal(4096, 1.2) contexts
+clipped to [16, 131072] with four sequences at 131,072, permuted pool with
+10% free blocks. The same run also times the Llama-3-8B-geometry batch of 64
+(lognormal(1024, 1.0) contexts in [1, 8192]) and reports it under
+per_workload.
 
 value = decode tokens per second = sequences per step / step time (all ranks'
 sequences over the slowest rank's time). Timing: CUDA events on the launch
 stream, L2 flushed before every timed launch (256 MiB written, then 256 MiB
-read, so L2 is cold and clean), outside the events. e2e: the same step through the public API from pinned host buffers,
-host->device copies of the step inputs and the device->host copy of the
-output inside the timed region.
+read, so L2 is cold and clean), outside the events. e2e: the same step
+through the public API from pinned host buffers, host->device copies of the
+step inputs and the device->host copy of the output inside the timed region.
 
---impl reference times the oracle (plain numpy, float64) on a bounded sample
-of the same workload on the host cores.
+cpu_baseline and --impl reference time the oracle (plain numpy, float64) on
+the same sample of the workload's sequences, one process per host core.
 """
 from __future__ import annotations
 
@@ -50,7 +53,10 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="llama3_8b_b64")
+    ap.add_argument("--workload", default="llama33_70b_b256")
+    ap.add_argument("--also", default="llama3_8b_b64",
+                    help="comma-separated workloads also timed in the same run (per_workload); 'none' for none")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="least wall time of the timed oracle passes")
     ap.add_argument("--num-ctas", type=int, default=0)
     ap.add_argument("--block-tokens", type=int, default=16, help="cache block size (8, 16, 32 or 64)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -128,20 +134,235 @@ def kernel_hash():
 
 
 def recorded_traffic(workload, units):
-    """DRAM bytes per launch from a committed ncu capture, scaled to this
-    launch by context tokens, or None if absent or the kernel changed."""
+    """DRAM bytes per launch from a committed ncu capture of this workload,
+    (value, "measured"); else one of another workload scaled to this launch by
+    context tokens, (value, "scaled from <workload>"); else (None, reason).
+    Nothing applies once the kernel's device code has changed."""
     try:
         with open(TRAFFIC_FILE) as f:
             rec = json.load(f)
     except (OSError, ValueError):
-        return None
+        return None, "no traffic record"
     if rec.get("kernel_sha256_16") != kernel_hash():
-        return None
-    if rec.get("workload") == workload:
-        return float(rec["dram_bytes_per_launch"])
-    if rec.get("context_tokens"):
-        return float(rec["dram_bytes_per_launch"]) * units / float(rec["context_tokens"])
-    return None
+        return None, "kernel changed since the traffic record"
+    records = rec.get("records", {})
+    if workload in records:
+        return float(records[workload]["dram_bytes_per_launch"]), "measured"
+    for name, r in sorted(records.items()):
+        if r.get("context_tokens"):
+            return float(r["dram_bytes_per_launch"]) * units / float(r["context_tokens"]), f"scaled from {name}"
+    return None, "no traffic record"
+
+
+# ---------------------------------------------------------------------------
+# The oracle on the host cores: cpu_baseline and the reference arm.
+
+def oracle_sample(ctx):
+    """Rows the oracle baseline times: every 4th sequence by context length,
+    plus the longest contexts (up to four rows at the maximum)."""
+    ctx = np.asarray(ctx)
+    order = np.argsort(ctx, kind="stable")
+    rows = set(int(r) for r in order[::4])
+    rows.update(int(r) for r in np.flatnonzero(ctx == ctx.max())[:4])
+    return sorted(rows)
+
+
+def split_rows(rows, ctx, n):
+    """Rows dealt to n workers, longest first to the least loaded (about
+    equal context tokens each); empty shares are dropped."""
+    shares = [[] for _ in range(n)]
+    load = [0] * n
+    for r in sorted(rows, key=lambda r: -int(ctx[r])):
+        i = load.index(min(load))
+        shares[i].append(r)
+        load[i] += int(ctx[r]) + 1
+    return [sorted(x) for x in shares if x]
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_batch_ctx(w):
+    """Context lengths of the workload's decode step, from the oracle's block
+    manager (bookkeeping only, no pool)."""
+    from oracle import scenario
+    from oracle.block_manager import BlockManager
+    bm = BlockManager(w.pool_blocks, w.block_tokens, w.free_order)
+    scenario._apply_events(w, bm)
+    bm.prepare_append(w.batch)
+    return np.array([bm.context_len(s) for s in w.batch], dtype=np.int64)
+
+
+def _oracle_worker(conn, name, seed, rows, extra):
+    """One host core's share of the oracle step: its rows' inputs are built
+    once (untimed), then each request runs the step -- the block copies, the
+    rows' appends and their attention -- and answers with its duration."""
+    from oracle import cache_ops, paged_attention, scenario
+    from workloads import make_workload
+    try:
+        w = make_workload(name, seed=seed, **extra)
+        if any(ev[0] == "history" for ev in w.events):
+            ref = scenario.replay(w, attend=False)  # small pools: the whole pool
+            q, k_new, v_new = w.step_inputs()
+            inp = dict(q=q[rows], k_new=k_new[rows], v_new=v_new[rows], k_pool=ref["k_pool"], v_pool=ref["v_pool"],
+                       pairs=ref["pairs"], slots=[ref["slots"][r] for r in rows], tables=ref["tables"][rows],
+                       ctx=ref["ctx"][rows])
+        else:
+            inp = scenario.sampled_inputs(w, rows)
+        conn.send(("ready", int(np.sum(inp["ctx"]))))
+        while True:
+            cmd = conn.recv()
+            if cmd == "stop":
+                break
+            t0 = time.perf_counter()
+            cache_ops.copy_blocks(inp["k_pool"], inp["v_pool"], inp["pairs"])
+            cache_ops.append_kv(inp["k_pool"], inp["v_pool"], inp["k_new"], inp["v_new"], inp["slots"])
+            out = paged_attention.paged_decode_attention(inp["q"], inp["k_pool"], inp["v_pool"], inp["tables"],
+                                                         inp["ctx"], w.scale)
+            el = time.perf_counter() - t0
+            conn.send(("done", el, out if cmd == "out" else None))
+    except Exception as e:  # reported to the parent, which raises
+        conn.send(("error", repr(e)))
+    finally:
+        conn.close()
+
+
+class OracleCores:
+    """The oracle step on a sample of a workload's sequences, one spawned
+    process per host core (each builds its rows' inputs once). step() runs
+    one pass over the sample on every worker at once and returns its wall
+    time and the sum of the workers' busy times (what one core would take)."""
+
+    def __init__(self, name, seed, rows, ctx, workers, extra=None):
+        import multiprocessing as mp
+        env = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
+        for k in env:
+            os.environ[k] = "1"  # one thread per worker process
+        ctxm = mp.get_context("spawn")
+        self.rows = list(rows)
+        self.shares = split_rows(self.rows, ctx, max(1, workers))
+        self.procs, self.conns = [], []
+        try:
+            for share in self.shares:
+                a, b = ctxm.Pipe()
+                p = ctxm.Process(target=_oracle_worker, args=(b, name, seed, share, extra or {}), daemon=True)
+                p.start()
+                self.procs.append(p)
+                self.conns.append(a)
+        finally:
+            for k, v in env.items():
+                if v is None:
+                    os.environ.pop(k, None)
+                else:
+                    os.environ[k] = v
+        self.context_tokens = None
+
+    @property
+    def workers(self):
+        return len(self.shares)
+
+    def _recv(self, c):
+        msg = c.recv()
+        if msg[0] == "error":
+            raise RuntimeError(f"oracle worker failed: {msg[1]}")
+        return msg
+
+    def wait_ready(self):
+        if self.context_tokens is None:
+            self.context_tokens = sum(self._recv(c)[1] for c in self.conns)
+        return self
+
+    def step(self, want_out=False):
+        self.wait_ready()
+        t0 = time.perf_counter()
+        for c in self.conns:
+            c.send("out" if want_out else "run")
+        msgs = [self._recv(c) for c in self.conns]
+        wall = time.perf_counter() - t0
+        busy = sum(m[1] for m in msgs)
+        if want_out:
+            out = {}
+            for share, m in zip(self.shares, msgs):
+                for i, r in enumerate(share):
+                    out[r] = m[2][i]
+            return wall, busy, out
+        return wall, busy
+
+    def close(self):
+        for c in self.conns:
+            try:
+                c.send("stop")
+            except OSError:
+                pass
+        for p in self.procs:
+            p.join(timeout=30)
+            if p.is_alive():
+                p.terminate()
+
+    def describe(self, w):
+        return (f"{len(self.rows)} of {w.batch_size} sequences (every 4th by context length and the longest; "
+                f"{self.context_tokens} context tokens), one process per host core ({self.workers}); "
+                "numpy float64 oracle, as committed")
+
+
+def time_oracle(pool, min_seconds, w):
+    """Passes of the oracle step over the sample until min_seconds of wall
+    time; the cpu_baseline record."""
+    pool.wait_ready()
+    pool.step()  # warm-up pass
+    walls, busy = [], []
+    while sum(walls) < min_seconds:
+        a, b = pool.step()
+        walls.append(a)
+        busy.append(b)
+    n = len(pool.rows)
+    return {"value": n * len(walls) / sum(walls), "unit": UNIT, "cores": pool.workers, "kind": "oracle",
+            "sample": pool.describe(w) + f"; {len(walls)} timed passes, {sum(walls):.1f} s",
+            "single_core_value": n * len(busy) / sum(busy),
+            "single_core_note": "the same passes' summed per-process busy time (the time one core would take)"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_info()
+    if rank != 0:
+        return
+    from workloads import make_workload
+
+    w = make_workload(args.workload)
+    ctx = oracle_batch_ctx(w)
+    rows = oracle_sample(ctx)
+    pool = OracleCores(args.workload, 0, rows, ctx, min(host_cores(), len(rows)))
+    try:
+        pool.wait_ready()
+        for _ in range(args.warmup):
+            pool.step()
+        walls, busy = [], []
+        for _ in range(args.steps):
+            a, b = pool.step()
+            walls.append(a)
+            busy.append(b)
+    finally:
+        pool.close()
+    el = sum(walls)
+    value = len(rows) * args.steps / el
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch_size, "q_heads": w.num_q_heads,
+                   "kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_tokens": 16,
+                   "sample_sequences": len(rows), "sample_context_tokens": pool.context_tokens},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": pool.workers, "kind": "oracle",
+                         "sample": pool.describe(w) + "; one pass over the sample per step",
+                         "single_core_value": len(rows) * args.steps / sum(busy)},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
 
 
 class L2Flush:
@@ -259,89 +480,15 @@ class ClockSampler:
                 "samples": len(self.samples), "source": "nvml" if self._nvml else "nvidia-smi"}
 
 
-def cpu_oracle_time(w, rows_budget_s=(10.0, 30.0)):
-    """The oracle's decode step (append + attention) on a sample of the
-    workload's sequences, repeated until at least rows_budget_s[0] seconds."""
-    from oracle import cache_ops, paged_attention, scenario
-
-    ref = scenario.replay(w, attend=False)
-    q, k_new, v_new = w.step_inputs()
-    k_pool, v_pool = ref["k_pool"], ref["v_pool"]
-    order = np.argsort(ref["ctx"])  # a spread of lengths: every 4th sequence by length
-    sample = sorted(order[::4].tolist())
-    done, t0 = 0, time.perf_counter()
-    while True:
-        cache_ops.append_kv(k_pool, v_pool, k_new[sample], v_new[sample], [ref["slots"][i] for i in sample])
-        paged_attention.paged_decode_attention(q, k_pool, v_pool, ref["tables"], ref["ctx"], w.scale, seqs=sample)
-        done += len(sample)
-        el = time.perf_counter() - t0
-        if el >= rows_budget_s[0] or el >= rows_budget_s[1]:
-            break
-    return {"value": done / el, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{len(sample)} of {w.batch_size} sequences (every 4th by context length, "
-                      f"{int(ref['ctx'][sample].sum())} context tokens), repeated for {el:.1f} s; "
-                      "numpy float64, single thread"}
-
-
-def run_reference(args):
-    rank, world, _ = dist_info()
-    if rank != 0:
-        return
-    from workloads import make_workload
-    from oracle import cache_ops, paged_attention, scenario
-
-    w = make_workload(args.workload)
-    ref = scenario.replay(w, attend=False)
-    q, k_new, v_new = w.step_inputs()
-    order = np.argsort(ref["ctx"])
-    sample = sorted(order[::8].tolist())  # each step: every 8th sequence by length
-
-    def step():
-        cache_ops.append_kv(ref["k_pool"], ref["v_pool"], k_new[sample], v_new[sample],
-                            [ref["slots"][i] for i in sample])
-        paged_attention.paged_decode_attention(q, ref["k_pool"], ref["v_pool"], ref["tables"], ref["ctx"],
-                                               w.scale, seqs=sample)
-
-    for _ in range(args.warmup):
-        step()
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        step()
-    el = time.perf_counter() - t0
-    value = len(sample) * args.steps / el
-    line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic",
-        "config": {"workload": w.name, "batch": w.batch_size, "q_heads": w.num_q_heads,
-                   "kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_tokens": 16,
-                   "sample_sequences": len(sample)},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": f"{len(sample)} of {w.batch_size} sequences per step (every 8th by "
-                                   "context length); numpy float64, single thread"},
-        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-    }
-    print(json.dumps(line), flush=True)
-
-
-def run_ours(args):
+def measure(pkv, name, args, rank, world, local, flush, e2e_on=True):
+    """One workload on this rank's GPU: the timed decode steps, the step's
+    kernels alone, end to end through the host-buffer call, and the roofline
+    of the attention launch. Returns the measurements for the JSON line."""
     import torch
     import torch.distributed as dist
 
-    rank, world, local = dist_info()
-    torch.cuda.set_device(local)
-    if world > 1:
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    if rank == 0 or world == 1:
-        from __graft_entry__ import _build_module
-        _build_module().build()
-    if world > 1:
-        dist.barrier()
-    import paged_kv_cache_49_gb300 as pkv
-
     extra = {} if args.block_tokens == 16 else {"block_tokens": args.block_tokens}
-    w = rank_workload(args.workload, rank, **extra)
+    w = rank_workload(name, rank, **extra)
     eng = pkv.PagedKVEngine(w.pool_blocks, w.num_q_heads, w.num_kv_heads, w.head_dim, free_order=w.free_order,
                             block_tokens=w.block_tokens)
     eng.load_workload_pool(w)
@@ -351,7 +498,6 @@ def run_ours(args):
     ctx = sb.ctx.cpu().numpy()
     B = w.batch_size
     stream = torch.cuda.current_stream()
-    flush = L2Flush()
 
     for _ in range(args.warmup):
         eng.run_step(sb, w.scale, args.num_ctas)
@@ -365,20 +511,13 @@ def run_ours(args):
     # kernel issued first keeps the GPU busy while the host enqueues all of
     # it, so host submission latency does not land inside device timings
     # (the effect CUDA-graph replay of a decode step has in a server).
-    ev_step = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
-    ev_attn = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
-    # the step's cache kernels alone too (both idempotent for fixed inputs)
-    ev_app = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
-    ev_copy = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps if sb.num_pairs else 0)]
+    ev = lambda n: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    ev_step, ev_attn, ev_app = ev(args.steps), ev(args.steps), ev(args.steps)
+    ev_copy = ev(args.steps if sb.num_pairs else 0)
     # batches whose shared prefixes save enough reads: cascade attention too
     cas = eng.cascade_for(sb)
     cas_out = torch.empty_like(sb.out) if cas else None
-    ev_cas = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps if cas else 0)]
+    ev_cas = ev(args.steps if cas else 0)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -397,7 +536,7 @@ def run_ours(args):
             pkv.attn_decode(sb.q, eng.k_cache, eng.v_cache, sb.tables, sb.ctx, w.scale, sb.out,
                             sb.workspace, args.num_ctas)
             ev_attn[i][1].record(stream)
-        for i, (e0, e1) in enumerate(ev_app):
+        for i, (e0, e1) in enumerate(ev_app):  # the step's cache kernels alone (idempotent for fixed inputs)
             flush(i + 2)
             e0.record(stream)
             pkv.append(sb.k, sb.v, sb.slots, eng.k_cache, eng.v_cache, eng.error)
@@ -418,15 +557,11 @@ def run_ours(args):
     step_ms = [a.elapsed_time(b) for a, b in ev_step]
     attn_ms = [a.elapsed_time(b) for a, b in ev_attn]
     ms = max_over_ranks(statistics.mean(step_ms), world)
-    value = whole_job_rate(B, world, ms)
-    step_stats = {"min": min(step_ms), "median": statistics.median(step_ms), "max": max(step_ms)}
-    attn_stats = {"min": min(attn_ms), "median": statistics.median(attn_ms), "max": max(attn_ms)}
 
     def stats_of(evs):
         t = [a.elapsed_time(b) for a, b in evs]
         return {"min": min(t), "median": statistics.median(t), "max": max(t)} if t else None
 
-    app_stats, copy_stats, cas_stats = stats_of(ev_app), stats_of(ev_copy), stats_of(ev_cas)
     launches = (args.steps * (2 + (1 if sb.num_pairs else 0)) + args.steps + len(ev_app) + len(ev_copy)
                 + 3 * len(ev_cas))
     if cas is not None:
@@ -443,7 +578,7 @@ def run_ours(args):
     # step's kernels, and the output rows written back to pinned host memory
     # by the attention itself.
     e2e = None
-    if not args.no_e2e:
+    if e2e_on:
         hs = pkv.HostStep(eng, B, sb.tables.shape[1], max_pairs=max(1, sb.num_pairs))
         h2d = hs.pack(sb.q.cpu(), sb.k.cpu(), sb.v.cpu(), sb.slots.cpu(), sb.tables.cpu(), sb.ctx.cpu(),
                       sb.pairs.cpu() if sb.num_pairs else None)
@@ -473,19 +608,17 @@ def run_ours(args):
             hs.run(w.scale, args.num_ctas)
         g_ms = timed(graph.replay)
         e2e["graph_replay"] = {"value": whole_job_rate(B, world, g_ms), "ms_per_step": g_ms}
-
-    if rank != 0:
-        if world > 1:
-            dist.destroy_process_group()
-        return
+        # timed calls, eager and replayed: staging, block copy (if any), append, attention
+        launches += 2 * args.steps * (3 + (1 if sb.num_pairs else 0))
 
     abytes = algorithmic_bytes(ctx, w.num_q_heads, w.num_kv_heads, block_tokens=w.block_tokens)
     ubytes = unique_kv_bytes(sb.tables.cpu().numpy(), ctx, w.num_kv_heads, block_tokens=w.block_tokens)
     attn_s = statistics.mean(attn_ms) * 1e-3
     peak, peak_kind = measured_peak_gbs()
     achieved = abytes / attn_s / 1e9
+    traffic, traffic_src = recorded_traffic(w.name, int(ctx.sum()))
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "traffic": recorded_traffic(w.name, int(ctx.sum())),
+                "frac": achieved / peak, "traffic": traffic, "traffic_source": traffic_src,
                 "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs copy bandwidth)",
                 "kernel": "pkv::attn::decode_kernel", "algorithmic_bytes_per_launch": abytes,
                 "attn_ms": attn_s * 1e3, "attn_ms_min": min(attn_ms), "frac_of_nominal_8tbs": achieved / 8000.0,
@@ -496,22 +629,72 @@ def run_ours(args):
                                "saved_kv_bytes": pkv.cascade_saved_bytes(cas.groups, w.num_kv_heads),
                                "logical_gbs": abytes / cas_s / 1e9, "unique_kv_gbs": ubytes / cas_s / 1e9,
                                "frac_unique_of_measured": ubytes / cas_s / 1e9 / peak}
-    cpu = None
-    if not args.no_cpu_baseline and world == 1:
-        cpu = cpu_oracle_time(w)
-    line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+    res = {
+        "w": w, "value": whole_job_rate(B, world, ms), "ms_per_step": ms, "e2e": e2e, "gpu_launches": launches,
+        "roofline": roofline, "clocks": clk.summary(),
+        "timing_ms": {"step": stats_of(ev_step), "attention_alone": stats_of(ev_attn),
+                      "append_alone": stats_of(ev_app), "block_copy_alone": stats_of(ev_copy),
+                      "attention_cascade": stats_of(ev_cas)},
         "config": {"workload": w.name, "batch": B, "q_heads": w.num_q_heads, "kv_heads": w.num_kv_heads,
                    "head_dim": w.head_dim, "block_tokens": w.block_tokens, "context_tokens": int(ctx.sum()),
                    "pool_blocks": w.pool_blocks, "cow_pairs_per_step": sb.num_pairs,
-                   "num_ctas": args.num_ctas or pkv.default_ctas(B), "l2": "flushed before each timed launch (256 MiB write, then 256 MiB read: cold and clean)",
+                   "num_ctas": args.num_ctas or pkv.default_ctas(B),
+                   "l2": "flushed before each timed launch (256 MiB write, then 256 MiB read: cold and clean)",
                    "parallelism": f"replicas x{world}"},
-        "clocks": clk.summary(), "e2e": e2e, "gpu_launches": launches, "roofline": roofline,
-        "timing_ms": {"step": step_stats, "attention_alone": attn_stats, "append_alone": app_stats,
-                      "block_copy_alone": copy_stats, "attention_cascade": cas_stats},
-        "cpu_baseline": cpu,
+    }
+    return res
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    rank, world, local = dist_info()
+    # The oracle's host processes (rank 0, one GPU) are spawned first, so
+    # that they build their inputs while the GPU side loads its pool.
+    pool = None
+    if not args.no_cpu_baseline and world == 1:
+        from workloads import make_workload
+        w0 = make_workload(args.workload) if args.block_tokens == 16 else None
+        if w0 is not None:
+            ctx0 = oracle_batch_ctx(w0)
+            rows = oracle_sample(ctx0)
+            pool = OracleCores(args.workload, 0, rows, ctx0, min(host_cores(), len(rows)))
+    try:
+        torch.cuda.set_device(local)
+        if world > 1:
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        if rank == 0 or world == 1:
+            from __graft_entry__ import _build_module
+            _build_module().build()
+        if world > 1:
+            dist.barrier()
+        import paged_kv_cache_49_gb300 as pkv
+
+        flush = L2Flush()
+        head = measure(pkv, args.workload, args, rank, world, local, flush, e2e_on=not args.no_e2e)
+        others = {}
+        for name in [x for x in args.also.split(",") if x and x != "none" and x != args.workload]:
+            torch.cuda.empty_cache()  # the previous workload's pool
+            m = measure(pkv, name, args, rank, world, local, flush, e2e_on=not args.no_e2e)
+            others[name] = {k: m[k] for k in ("value", "ms_per_step", "e2e", "roofline", "timing_ms", "clocks",
+                                              "config", "gpu_launches")}
+        cpu = time_oracle(pool, args.cpu_seconds, head["w"]) if pool is not None and rank == 0 else None
+    finally:
+        if pool is not None:
+            pool.close()
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    line = {
+        "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": head["config"],
+        "clocks": head["clocks"], "e2e": head["e2e"],
+        "gpu_launches": head["gpu_launches"] + sum(o["gpu_launches"] for o in others.values()),
+        "roofline": head["roofline"], "timing_ms": head["timing_ms"], "cpu_baseline": cpu,
+        "per_workload": others,
     }
     print(json.dumps(line), flush=True)
     if world > 1:

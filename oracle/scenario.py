@@ -72,11 +72,17 @@ def replay(w, attend: bool = True):
     return res
 
 
-def replay_sampled(w, sample_rows):
-    """Attention for the batch rows in `sample_rows` only, regenerating just
-    the pool blocks those rows read. For workloads without history events
-    (every token before the step is pool content). Returns (out_rows float64
-    [len(sample_rows), Hq, D], the full-replay bookkeeping dict without pools)."""
+def sampled_inputs(w, sample_rows):
+    """The decode step's inputs restricted to the batch rows in `sample_rows`,
+    regenerating just the pool blocks those rows read (for workloads without
+    history events: every token before the step is pool content). Returns a
+    dict: q, k_new, v_new (the sampled rows'), k_pool / v_pool (the needed
+    blocks before the step's copies and appends, renumbered), pairs and slots
+    (the step's copies and the sampled rows' appends in that numbering, -1
+    for an append outside it), tables and ctx (the sampled rows'),
+    loc_slots_all (every batch row's append in that numbering) and the full
+    batch's bookkeeping (bm, all_slots, all_pairs, all_tables, all_ctx, all_q,
+    all_k_new, all_v_new)."""
     if any(ev[0] == "history" for ev in w.events):
         raise ValueError("sampled replay needs a workload without history appends")
     bm = BlockManager(w.pool_blocks, w.block_tokens, w.free_order)
@@ -86,27 +92,41 @@ def replay_sampled(w, sample_rows):
     tables = padded_tables(bm, w.batch)
     ctx = np.array([bm.context_len(s) for s in w.batch], dtype=np.int64)
     rows = [int(r) for r in sample_rows]
+    b = w.block_tokens
     # physical blocks the sampled rows read, plus sources copied into them
     need = set()
     for r in rows:
-        need.update(int(b) for b in tables[r, : -(-int(ctx[r]) // w.block_tokens)])
+        need.update(int(x) for x in tables[r, : -(-int(ctx[r]) // b)])
     need.update(s for s, d in pairs if d in need)
     need = sorted(need)
-    remap = {b: i for i, b in enumerate(need)}
-    k_loc = w.pool_blocks_at("k", need)
-    v_loc = w.pool_blocks_at("v", need)
+    remap = {blk: i for i, blk in enumerate(need)}
     loc_pairs = [(remap[s], remap[d]) for s, d in pairs if d in remap]
-    cache_ops.copy_blocks(k_loc, v_loc, loc_pairs)
-    b = w.block_tokens
-    loc_slots = []
-    for s in slots:
-        blk = s // b
-        loc_slots.append(remap[blk] * b + s % b if blk in remap else -1)
-    cache_ops.append_kv(k_loc, v_loc, k_new, v_new, loc_slots)
+    # every batch row's append in the new numbering (-1 outside it)
+    loc_slots_all = []
+    for sl in slots:
+        blk = sl // b
+        loc_slots_all.append(remap[blk] * b + sl % b if blk in remap else -1)
     loc_tables = np.full((len(rows), tables.shape[1]), -1, dtype=np.int32)
     for i, r in enumerate(rows):
         n = -(-int(ctx[r]) // b)
         loc_tables[i, :n] = [remap[int(x)] for x in tables[r, :n]]
+    return dict(q=q[rows], k_new=k_new[rows], v_new=v_new[rows],
+                k_pool=w.pool_blocks_at("k", need), v_pool=w.pool_blocks_at("v", need),
+                pairs=loc_pairs, slots=[loc_slots_all[r] for r in rows], tables=loc_tables, ctx=ctx[rows],
+                loc_slots_all=loc_slots_all, all_k_new=k_new, all_v_new=v_new,
+                bm=bm, all_slots=slots, all_pairs=pairs, all_tables=tables, all_ctx=ctx, all_q=q)
+
+
+def replay_sampled(w, sample_rows):
+    """Attention for the batch rows in `sample_rows` only, regenerating just
+    the pool blocks those rows read. For workloads without history appends
+    (every token before the step is pool content). Returns (out_rows float64
+    [len(sample_rows), Hq, D], the full-replay bookkeeping dict without pools)."""
+    inp = sampled_inputs(w, sample_rows)
+    k_loc, v_loc = inp["k_pool"], inp["v_pool"]
+    cache_ops.copy_blocks(k_loc, v_loc, inp["pairs"])
+    cache_ops.append_kv(k_loc, v_loc, inp["all_k_new"], inp["all_v_new"], inp["loc_slots_all"])
     out = paged_attention.paged_decode_attention(
-        q[rows], k_loc, v_loc, loc_tables, ctx[rows], w.scale)
-    return out, dict(bm=bm, slots=slots, pairs=pairs, tables=tables, ctx=ctx, q=q)
+        inp["q"], k_loc, v_loc, inp["tables"], inp["ctx"], w.scale)
+    return out, dict(bm=inp["bm"], slots=inp["all_slots"], pairs=inp["all_pairs"], tables=inp["all_tables"],
+                     ctx=inp["all_ctx"], q=inp["all_q"])

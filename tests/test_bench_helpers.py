@@ -31,18 +31,21 @@ def test_unique_kv_bytes_count_shared_blocks_once():
 
 
 def test_recorded_traffic_applies_only_to_the_profiled_kernel(tmp_path, monkeypatch):
-    rec = {"kernel_sha256_16": bench.kernel_hash(), "workload": "llama3_8b_b64", "context_tokens": 1000,
-           "dram_bytes_per_launch": 5.0e8}
+    rec = {"kernel_sha256_16": bench.kernel_hash(),
+           "records": {"llama3_8b_b64": {"context_tokens": 1000, "dram_bytes_per_launch": 5.0e8}}}
     path = tmp_path / "traffic.json"
     path.write_text(json.dumps(rec))
     monkeypatch.setattr(bench, "TRAFFIC_FILE", str(path))
-    assert bench.recorded_traffic("llama3_8b_b64", 1234) == 5.0e8
-    assert bench.recorded_traffic("other", 2000) == 1.0e9  # scaled by context tokens
+    assert bench.recorded_traffic("llama3_8b_b64", 1234) == (5.0e8, "measured")
+    assert bench.recorded_traffic("other", 2000) == (1.0e9, "scaled from llama3_8b_b64")  # by context tokens
+    rec["records"]["other"] = {"context_tokens": 3000, "dram_bytes_per_launch": 7.0e8}
+    path.write_text(json.dumps(rec))
+    assert bench.recorded_traffic("other", 2000) == (7.0e8, "measured")  # its own capture wins
     rec["kernel_sha256_16"] = "0" * 16  # captured from other device code
     path.write_text(json.dumps(rec))
-    assert bench.recorded_traffic("llama3_8b_b64", 1234) is None
+    assert bench.recorded_traffic("llama3_8b_b64", 1234)[0] is None
     monkeypatch.setattr(bench, "TRAFFIC_FILE", str(tmp_path / "absent.json"))
-    assert bench.recorded_traffic("llama3_8b_b64", 1234) is None
+    assert bench.recorded_traffic("llama3_8b_b64", 1234)[0] is None
 
 
 def test_kernel_hash_covers_the_device_sources_only():
@@ -50,3 +53,40 @@ def test_kernel_hash_covers_the_device_sources_only():
     assert names == ["pkv_decode_kernel.cuh", "pkv_ptx.cuh"]
     h = bench.kernel_hash()
     assert len(h) == 16 and int(h, 16) >= 0
+
+
+def test_oracle_sample_and_row_split():
+    ctx = np.array([131072, 5, 131072, 900, 17, 4000, 131072, 33, 131072, 131072, 60])
+    rows = bench.oracle_sample(ctx)
+    assert rows == sorted(set(rows))
+    assert {0, 2, 6, 8} <= set(rows)  # the first four rows at the maximum
+    order = np.argsort(ctx, kind="stable")
+    assert set(order[::4].tolist()) <= set(rows)
+    shares = bench.split_rows(rows, ctx, 3)
+    assert sorted(r for sh in shares for r in sh) == rows  # every row exactly once
+    assert len(shares) == 3
+    assert len(bench.split_rows([1, 4], ctx, 8)) == 2  # no empty shares
+
+
+def test_oracle_cores_equal_the_single_process_oracle():
+    """The all-core baseline runs the committed oracle unchanged: its outputs
+    over the sample equal the oracle's own replay, row for row."""
+    from oracle import scenario
+    from workloads import make_workload
+
+    for name in ("tiny", "tiny_nan"):
+        w = make_workload(name)
+        ctx = bench.oracle_batch_ctx(w)
+        ref = scenario.replay(w)
+        assert np.array_equal(ctx, ref["ctx"])
+        rows = bench.oracle_sample(ctx)
+        pool = bench.OracleCores(name, 0, rows, ctx, 2)
+        try:
+            wall, busy, out = pool.step(want_out=True)
+            assert wall > 0 and busy > 0 and pool.workers == 2
+            for r in rows:
+                assert np.array_equal(out[r], ref["out"][r])
+            wall2, _, out2 = pool.step(want_out=True)  # a step is repeatable
+            assert all(np.array_equal(out2[r], out[r]) for r in rows)
+        finally:
+            pool.close()
