@@ -61,6 +61,8 @@ def parse():
     ap.add_argument("--block-tokens", type=int, default=16, help="cache block size (8, 16, 32 or 64)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-math-ab", action="store_true",
+                    help="skip timing the CUDA-core variant of the attention math beside the tensor-core kernel")
     return ap.parse_args()
 
 
@@ -518,6 +520,11 @@ def measure(pkv, name, args, rank, world, local, flush, e2e_on=True):
     cas = eng.cascade_for(sb)
     cas_out = torch.empty_like(sb.out) if cas else None
     ev_cas = ev(args.steps if cas else 0)
+    # the same attention with its per-tile math on the CUDA cores (group sizes
+    # 4 and 8): the measured alternative to the tensor cores
+    fma_ok = not args.no_math_ab and w.block_tokens == 16 and w.num_q_heads // w.num_kv_heads in (4, 8)
+    fma_out = torch.empty_like(sb.out) if fma_ok else None
+    ev_fma = ev(args.steps if fma_ok else 0)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -551,6 +558,12 @@ def measure(pkv, name, args, rank, world, local, flush, e2e_on=True):
             e0.record(stream)
             cas.decode(sb.q, eng.k_cache, eng.v_cache, sb.tables, sb.ctx, w.scale, cas_out)
             e1.record(stream)
+        for i, (e0, e1) in enumerate(ev_fma):
+            flush(i + 5)
+            e0.record(stream)
+            pkv.attn_decode_cuda_cores(sb.q, eng.k_cache, eng.v_cache, sb.tables, sb.ctx, w.scale, fma_out,
+                                       sb.workspace, args.num_ctas)
+            e1.record(stream)
         torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -563,7 +576,9 @@ def measure(pkv, name, args, rank, world, local, flush, e2e_on=True):
         return {"min": min(t), "median": statistics.median(t), "max": max(t)} if t else None
 
     launches = (args.steps * (2 + (1 if sb.num_pairs else 0)) + args.steps + len(ev_app) + len(ev_copy)
-                + 3 * len(ev_cas))
+                + 3 * len(ev_cas) + len(ev_fma))
+    if fma_ok and (fma_out.float() - sb.out.float()).abs().max().item() > 4e-2:
+        raise RuntimeError("the CUDA-core variant differs from the tensor-core kernel")
     if cas is not None:
         if cas.read_error():
             raise RuntimeError("device error word set by the cascade attention")
@@ -629,12 +644,18 @@ def measure(pkv, name, args, rank, world, local, flush, e2e_on=True):
                                "saved_kv_bytes": pkv.cascade_saved_bytes(cas.groups, w.num_kv_heads),
                                "logical_gbs": abytes / cas_s / 1e9, "unique_kv_gbs": ubytes / cas_s / 1e9,
                                "frac_unique_of_measured": ubytes / cas_s / 1e9 / peak}
+    if fma_ok:
+        fma_s = statistics.mean(a.elapsed_time(b) for a, b in ev_fma) * 1e-3
+        roofline["cuda_core_variant"] = {
+            "kernel": "pkv::attn::decode_kernel, per-tile math on FP32 FMA", "attn_ms": fma_s * 1e3,
+            "achieved": abytes / fma_s / 1e9, "frac": abytes / fma_s / 1e9 / peak,
+            "tensor_core_speedup": fma_s / attn_s}
     res = {
         "w": w, "value": whole_job_rate(B, world, ms), "ms_per_step": ms, "e2e": e2e, "gpu_launches": launches,
         "roofline": roofline, "clocks": clk.summary(),
         "timing_ms": {"step": stats_of(ev_step), "attention_alone": stats_of(ev_attn),
                       "append_alone": stats_of(ev_app), "block_copy_alone": stats_of(ev_copy),
-                      "attention_cascade": stats_of(ev_cas)},
+                      "attention_cascade": stats_of(ev_cas), "attention_cuda_cores": stats_of(ev_fma)},
         "config": {"workload": w.name, "batch": B, "q_heads": w.num_q_heads, "kv_heads": w.num_kv_heads,
                    "head_dim": w.head_dim, "block_tokens": w.block_tokens, "context_tokens": int(ctx.sum()),
                    "pool_blocks": w.pool_blocks, "cow_pairs_per_step": sb.num_pairs,
