@@ -147,6 +147,12 @@ size_t pkv_attn_workspace_size(int num_seqs, int num_kv_heads);
  * pkv_attn_decode leaves its counters at zero. */
 pkv_status pkv_attn_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
 
+/* Bytes at the start of every attention workspace that must hold zeros
+ * between calls: the 256-byte header (error word) and the merge counters
+ * (the same for every batch, KV-head count and grid). The bytes after them
+ * are scratch whose content never matters to the next call. */
+size_t pkv_attn_workspace_fixed_bytes(void);
+
 /*
  * pkv_attn_decode -- single-token decode attention through block tables.
  *

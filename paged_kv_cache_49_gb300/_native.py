@@ -43,7 +43,7 @@ EXPORTED = [
     "pkv_block_copy_ex", "pkv_bm_create_ex", "pkv_bm_admit_tokens", "pkv_bm_preempt", "pkv_bm_resume",
     "pkv_bm_newest_running", "pkv_bm_slots", "pkv_step_layout", "pkv_decode_step_host",
     "pkv_attn_cascade_workspace_size", "pkv_cascade_staging_size", "pkv_cascade_plan", "pkv_attn_decode_cascade",
-    "pkv_attn_decode_wait_test", "pkv_attn_decode_cuda_cores",
+    "pkv_attn_decode_wait_test", "pkv_attn_decode_cuda_cores", "pkv_attn_workspace_fixed_bytes",
 ]
 BLOCK_SIZES = (8, 16, 32, 64)
 
@@ -102,6 +102,7 @@ def _load() -> ctypes.CDLL:
         "pkv_attn_decode_ex": (i32, [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, f32, i32, vp, sz, vp, vp]),
         "pkv_attn_workspace_size": (sz, [i32, i32]),
         "pkv_attn_workspace_init": (i32, [vp, sz, vp]),
+        "pkv_attn_workspace_fixed_bytes": (sz, []),
         "pkv_attn_decode": (i32, [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, f32, i32, vp, sz, vp, vp]),
         "pkv_attn_default_ctas": (i32, [i32]),
         "pkv_attn_decode_cuda_cores": (i32, [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, f32, i32, vp, sz, vp,
@@ -259,6 +260,12 @@ class AttentionWorkspace:
     @property
     def ptr(self) -> int:
         return self.tensor.data_ptr()
+
+    @staticmethod
+    def fixed_bytes() -> int:
+        """Leading bytes that must hold zeros between calls (error word,
+        merge counters); the rest is scratch."""
+        return int(_lib.pkv_attn_workspace_fixed_bytes())
 
     def error_word(self) -> torch.Tensor:
         return self.tensor[:4].view(torch.int32)

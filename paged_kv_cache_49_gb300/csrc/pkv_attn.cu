@@ -305,6 +305,8 @@ size_t pkv_attn_workspace_size(int num_seqs, int num_kv_heads) {
     return attn::workspace_bytes(grid);
 }
 
+size_t pkv_attn_workspace_fixed_bytes(void) { return attn::kWsFixed; }
+
 pkv_status pkv_attn_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
     if (!workspace || workspace_bytes < attn::kWsHeader) return PKV_EINVAL;
     const cudaError_t e = cudaMemsetAsync(workspace, 0, workspace_bytes, as_stream(stream));

@@ -250,9 +250,10 @@ def test_one_workspace_serves_any_launch_shape(pkv):
     so their merges run in two levels (group counters) as well as one."""
     rng = np.random.default_rng(21)
     D, dev = 128, "cuda"
-    # the workspace's counters: bytes [256, 256 + 2048 * 3 * 4) (a 256-byte
-    # header holds the error word); nothing after them has to start at zero
-    counters_end = 256 + ((pkv.MAX_CTAS * 3 * 4 + 255) // 256) * 256
+    # the header (error word) and the merge counters come first;
+    # nothing after them has to start at zero
+    counters_end = pkv.AttentionWorkspace.fixed_bytes()
+    assert counters_end % 256 == 0 and counters_end > 256
     shapes = []
     for B, Hq, Hkv, ctx in ((3, 16, 2, [5000, 37, 1200]), (40, 32, 8, None), (1, 8, 1, [20000])):
         if ctx is None:
