@@ -654,7 +654,6 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 for (int jj = 0; jj < cnt; ++jj) {
                     const int ya = __shfl_sync(0xffffffffu, y0, jj);
                     if (lane == 0 && mbar_wait(empty_bar(stage), sphase ^ 1u, abort_flag, p.err)) {
-                        fence_proxy_async_shared();  // the consumers' reads of the stage, before the copy over it
                         const uint32_t fb = full_bar(stage);
                         mbar_arrive_expect_tx(fb, kStageBytes);
                         const uint32_t dst = smem_u32(smem + stage * kStageBytes);
@@ -669,7 +668,12 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 }
             }
         }
-        if (lane == 0) {  // no copy may land after the CTA exits (bounded waits)
+        if (lane == 0) {  // no copy may land after the CTA exits (bounded waits; after an abort, a grace period first)
+            if (*abort_flag) {
+                const uint64_t t0 = global_timer_ns();
+                while (global_timer_ns() - t0 < kDrainGraceNs) {
+                }
+            }
             volatile int never = 0;
             for (int i = 0; i < kPfxStages; ++i)
                 if ((filled >> i) & 1u) mbar_wait(full_bar(i), (fill_par >> i) & 1u, &never, nullptr);
@@ -757,6 +761,7 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 ldmatrix_x4_trans(a, sv + (j >> 2) * kHalfBytes + v_row_off + ((chunk ^ v_sw) << 4));
                 mma_bf16_16816(o[j], a, pb0, pb1);
             }
+            fence_proxy_async_shared();  // this lane's reads of the stage, before the copy that will replace it
             __syncwarp();
             if (lane == 0 && landed) mbar_arrive(empty_bar(st));
         }

@@ -72,6 +72,8 @@ constexpr int kStages = 8;
 static_assert(kStages % kConsumerWarps == 0, "each stage must map to one consumer warp");
 static_assert((kConsumerWarps & (kConsumerWarps - 1)) == 0, "consumer warp count is a power of two");
 constexpr int kQSlots = 2;
+// After an abort, how long the producer waits before its drain (see there).
+constexpr uint64_t kDrainGraceNs = 100000;  // 100 us
 // Work partition cost of one (sequence, KV head) run beyond its tiles, in
 // tiles: what a piece's fixed work (its query rows, the hand-over between
 // consumer warps, the merge warp's combine and any cross-CTA merge) costs a
@@ -472,6 +474,7 @@ __device__ __forceinline__ void fma_consumer_warp(const Params& p, uint8_t* smem
                     }
                 }
             }
+            fence_proxy_async_shared();  // this lane's reads of the stage, before the copy that will replace it
             __syncwarp();
             if (lane == 0 && landed) mbar_arrive(empty_bar(st));
         }
@@ -742,7 +745,6 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                         }
                         // (tests of the bounded waits: past stop_at nothing is issued)
                         if (tile < stop_at && mbar_wait(empty_bar(stage), sphase ^ 1u, abort_flag, p.err)) {
-                            fence_proxy_async_shared();  // the consumer's reads of the stage, before the copy over it
                             const uint32_t fb = full_bar(stage);
                             mbar_arrive_expect_tx(fb, kStageBytes);
                             const uint32_t dst = smem_u32(smem + kOffStages + stage * kStageBytes);
@@ -774,9 +776,18 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         // Before this warp exits, wait (bounded, even after an abort) for the
         // last copy into each stage and query slot, so that no copy lands in
         // shared memory after the CTA has exited (every earlier copy has
-        // landed: see `filled`).
+        // landed: see `filled`). After an abort the record can miss a copy: a
+        // wait that gave up leaves a stage's phases one behind, and a later
+        // parity wait on that stage can pass for the phase before; so the
+        // producer then first waits a grace period far longer than any copy
+        // takes to land.
         if (!waited) griddep_wait();
         if (lane == 0) {
+            if (*abort_flag) {
+                const uint64_t t0 = global_timer_ns();
+                while (global_timer_ns() - t0 < kDrainGraceNs) {
+                }
+            }
             volatile int never = 0;
             for (int i = 0; i < kStages; ++i)
                 if ((filled >> i) & 1u) mbar_wait(full_bar(i), (fill_par >> i) & 1u, &never, nullptr);
@@ -1172,6 +1183,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 a[3] &= vmask23;
                 mma_bf16_16816(o[j], a, pb0, pb1);
             }
+            fence_proxy_async_shared();  // this lane's reads of the stage, before the copy that will replace it
             __syncwarp();
             if (lane == 0 && landed) mbar_arrive(empty_bar(st));
         }
