@@ -630,12 +630,8 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
 
     if (warp == kProducerWarp) {
         const uint64_t policy = policy_evict_first();
-        int stage = 0;
+        int stage = 0, issued = 0;
         uint32_t sphase = 0;
-        // stages that received a copy, and the phase parity of the last one
-        // (a stage is copied into only after its consumers saw its previous
-        // copy land, so that is the only copy that may be in flight)
-        uint32_t filled = 0, fill_par = 0;
         for (int it = blockIdx.x; it < p.num_items; it += gridDim.x) {
             const int4 item = p.items[it];
             const int g = item.z & 0xffff, n = item.z >> 16;
@@ -661,8 +657,7 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                         tma_load_2d(dst + kHalfBytes, &tm_k, 64, ya, fb, policy);
                         tma_load_2d(dst + kBlockBytes, &tm_v, 0, ya, fb, policy);
                         tma_load_2d(dst + kBlockBytes + kHalfBytes, &tm_v, 64, ya, fb, policy);
-                        filled |= 1u << stage;
-                        fill_par = (fill_par & ~(1u << stage)) | (sphase << stage);
+                        ++issued;
                     }
                     if (++stage == kPfxStages) { stage = 0; sphase ^= 1u; }
                 }
@@ -675,8 +670,8 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 }
             }
             volatile int never = 0;
-            for (int i = 0; i < kPfxStages; ++i)
-                if ((filled >> i) & 1u) mbar_wait(full_bar(i), (fill_par >> i) & 1u, &never, nullptr);
+            for (int i = max(0, issued - kPfxStages); i < issued; ++i)
+                mbar_wait(full_bar(i % kPfxStages), static_cast<uint32_t>((i / kPfxStages) & 1), &never, nullptr);
         }
         return;
     }

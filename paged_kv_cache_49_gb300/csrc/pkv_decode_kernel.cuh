@@ -685,14 +685,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         uint32_t sphase = 0, qphase = 0;
         int tile = 0;  // position in the CTA's stream of tiles
         const int stop_at = (p.stop_tiles >= 0 && blockIdx.x == 0) ? p.stop_tiles : INT_MAX;
-        // Lane 0's record of the copies it issued, for the drain before exit:
-        // bit i of `filled` = stage i received a copy, bit i of `fill_par` =
-        // the phase parity of its last one (q_filled / q_fill_par: the same
-        // for the query slots). A consumer releases a stage only after it saw
-        // the stage's copy land, and the producer copies into a stage only
-        // after its release, so every copy but the last into each stage has
-        // landed.
-        uint32_t filled = 0, fill_par = 0, q_filled = 0, q_fill_par = 0;
+        int issued = 0, q_issued = 0;  // copies issued into the stage ring and the query ring
         bool waited = false;  // griddep_wait done by this thread
         while (walk.next(pc)) {
             const int len = pc.len;
@@ -704,8 +697,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                         const __nv_bfloat16* src =
                             p.q + (static_cast<size_t>(pc.s) * p.num_q_heads + static_cast<size_t>(pc.g) * G) * kDim;
                         bulk_load(smem_u32(smem + kOffQ + qslot * kQBytes), src, G * kDim * 2, qfull_bar(qslot));
-                        q_filled |= 1u << qslot;
-                        q_fill_par = (q_fill_par & ~(1u << qslot)) | (qphase << qslot);
+                        ++q_issued;
                     }
                 }
                 if (++qslot == kQSlots) { qslot = 0; qphase ^= 1u; }
@@ -764,8 +756,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                                 tma_load_2d(dst + kBlockBytes + kHalfBytes, &tm_v, 64, ya, fb, policy);
                                 tma_load_2d(dst + kBlockBytes + kHalfBytes + kRow8, &tm_v, 64, yb, fb, policy);
                             }
-                            filled |= 1u << stage;
-                            fill_par = (fill_par & ~(1u << stage)) | (sphase << stage);
+                            ++issued;
                         }
                     }
                     if (++stage == kStages) { stage = 0; sphase ^= 1u; }
@@ -773,13 +764,14 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 }
             }
         }
-        // Before this warp exits, wait (bounded, even after an abort) for the
-        // last copy into each stage and query slot, so that no copy lands in
-        // shared memory after the CTA has exited (every earlier copy has
-        // landed: see `filled`). After an abort the record can miss a copy: a
-        // wait that gave up leaves a stage's phases one behind, and a later
-        // parity wait on that stage can pass for the phase before; so the
-        // producer then first waits a grace period far longer than any copy
+        // No copy may land in shared memory after the CTA has exited. Without
+        // an abort every copy issued was waited on by a consumer warp, and
+        // the wait below for the last copies into each ring (bounded) returns
+        // at once. After an abort a consumer may have given up on a copy
+        // still in flight, and the issued copies need not be a prefix of the
+        // stream (a wait that gave up leaves a stage's phases one behind, and
+        // a later parity wait on that stage can pass for the phase before),
+        // so the producer first waits a grace period far longer than any copy
         // takes to land.
         if (!waited) griddep_wait();
         if (lane == 0) {
@@ -789,10 +781,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 }
             }
             volatile int never = 0;
-            for (int i = 0; i < kStages; ++i)
-                if ((filled >> i) & 1u) mbar_wait(full_bar(i), (fill_par >> i) & 1u, &never, nullptr);
-            for (int i = 0; i < kQSlots; ++i)
-                if ((q_filled >> i) & 1u) mbar_wait(qfull_bar(i), (q_fill_par >> i) & 1u, &never, nullptr);
+            for (int i = max(0, issued - kStages); i < issued; ++i)
+                mbar_wait(full_bar(i % kStages), static_cast<uint32_t>((i / kStages) & 1), &never, nullptr);
+            for (int i = max(0, q_issued - kQSlots); i < q_issued; ++i)
+                mbar_wait(qfull_bar(i % kQSlots), static_cast<uint32_t>((i / kQSlots) & 1), &never, nullptr);
         }
         return;
     }
