@@ -595,8 +595,9 @@ def measure(pkv, name, args, rank, world, local, flush, e2e_on=True):
     e2e = None
     if e2e_on:
         hs = pkv.HostStep(eng, B, sb.tables.shape[1], max_pairs=max(1, sb.num_pairs))
-        h2d = hs.pack(sb.q.cpu(), sb.k.cpu(), sb.v.cpu(), sb.slots.cpu(), sb.tables.cpu(), sb.ctx.cpu(),
-                      sb.pairs.cpu() if sb.num_pairs else None)
+        hs.pack(sb.q.cpu(), sb.k.cpu(), sb.v.cpu(), sb.slots.cpu(), sb.tables.cpu(), sb.ctx.cpu(),
+                sb.pairs.cpu() if sb.num_pairs else None)
+        h2d = hs.h2d_bytes()  # what crosses the host link each step (table rows up to their live entries)
         d2h = hs.out_host.numel() * hs.out_host.element_size()
 
         def timed(run):

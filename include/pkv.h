@@ -354,8 +354,11 @@ pkv_status pkv_step_layout(int num_seqs, int num_q_heads, int num_kv_heads, int 
  * (device, [num_seqs][Hq][D] bf16), then one copy of those rows goes into
  * host_out. When host_packed is pinned host memory the device can address
  * (cudaHostAlloc / cudaHostRegister) and 16-byte aligned, a staging kernel
- * reads it across the host link (faster than a copy engine for a step's
- * ~1 MB); otherwise one asynchronous copy brings it. When host_out is such
+ * reads it across the host link (faster than a copy engine for a step's few
+ * MB), and of each block-table row only the entries up to
+ * ceil(context_len / 16) cross (no kernel reads past them; the rest of the
+ * row in device_staging keeps what it held); otherwise one asynchronous copy
+ * brings the whole buffer. When host_out is such
  * memory, the attention writes the rows there directly and device_out is not
  * touched (it must still be a valid device pointer). Everything is enqueued
  * on `stream` and checked before anything is enqueued: host_packed must not

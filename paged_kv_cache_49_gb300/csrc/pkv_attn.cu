@@ -266,24 +266,72 @@ pkv_status launch(const Launch& L, cudaStream_t stream, bool early) {
     return PKV_OK;
 }
 
-// Copy n16 16-byte words from pinned host memory that the device addresses
-// directly into device memory: every load crosses the host link at once, all
-// issued before any is stored (four per thread), where a copy engine takes
-// several times as long for the ~1 MB of a step's inputs.
+// Bring a step's packed inputs from pinned host memory that the device
+// addresses directly into device memory, in 16-byte words: every load
+// crosses the host link at once, all issued before any is stored (four per
+// thread), where a copy engine takes several times as long for a step's few
+// MB. Of the block tables only each row's entries up to ceil(context_len /
+// 16) cross (the kernels never read past them): a batch padded to its
+// longest row (the 70B batch: 256 rows of 8,192 entries, 8 MB, of which 0.6
+// MB are live) would otherwise move mostly padding.
+//  - blocks [0, dense_blocks): the words outside the table region, grid-
+//    stride;
+//  - the other blocks: one warp per task of up to kStageRowWords words of
+//    one table row (row r's tasks r * row_tasks ..), which reads the row's
+//    context length from the host buffer first.
 constexpr int kStageThreads = 256;
 constexpr int kStageUnroll = 4;
+constexpr int kStageRowWords = 32 * kStageUnroll;  // 2 KB of one row per warp task
 
-__global__ void __launch_bounds__(kStageThreads) stage_kernel(const uint4* src, uint4* __restrict__ dst, size_t n16) {
-    const size_t stride = static_cast<size_t>(gridDim.x) * kStageThreads;
-    size_t i = static_cast<size_t>(blockIdx.x) * kStageThreads + threadIdx.x;
-    for (; i + (kStageUnroll - 1) * stride < n16; i += kStageUnroll * stride) {
-        uint4 v[kStageUnroll];
+struct StageArgs {
+    const uint4* src;
+    uint4* dst;
+    size_t n16;                          // words in the packed buffer
+    size_t tab_lo, tab_hi;               // the table region, in words
+    size_t tab_byte0;                    // its first byte
+    const int32_t* ctx;                  // context lengths in the host buffer (device view)
+    int rows, row_entries, row_tasks;    // table rows, entries per row, warp tasks per row
+    int dense_blocks;
+};
+
+__global__ void __launch_bounds__(kStageThreads) stage_kernel(const StageArgs a) {
+    if (static_cast<int>(blockIdx.x) < a.dense_blocks) {
+        const size_t n = a.n16 - (a.tab_hi - a.tab_lo);  // words outside the table region
+        const size_t stride = static_cast<size_t>(a.dense_blocks) * kStageThreads;
+        auto at = [&](size_t i) { return i < a.tab_lo ? i : i + (a.tab_hi - a.tab_lo); };
+        size_t i = static_cast<size_t>(blockIdx.x) * kStageThreads + threadIdx.x;
+        for (; i + (kStageUnroll - 1) * stride < n; i += kStageUnroll * stride) {
+            uint4 v[kStageUnroll];
 #pragma unroll
-        for (int u = 0; u < kStageUnroll; ++u) v[u] = src[i + u * stride];
+            for (int u = 0; u < kStageUnroll; ++u) v[u] = a.src[at(i + u * stride)];
 #pragma unroll
-        for (int u = 0; u < kStageUnroll; ++u) dst[i + u * stride] = v[u];
+            for (int u = 0; u < kStageUnroll; ++u) a.dst[at(i + u * stride)] = v[u];
+        }
+        for (; i < n; i += stride) a.dst[at(i)] = a.src[at(i)];
+        return;
     }
-    for (; i < n16; i += stride) dst[i] = src[i];
+    const int lane = threadIdx.x & 31;
+    const long long task = (static_cast<long long>(blockIdx.x) - a.dense_blocks) * (kStageThreads / 32) + (threadIdx.x >> 5);
+    if (task >= static_cast<long long>(a.rows) * a.row_tasks) return;
+    const int r = static_cast<int>(task / a.row_tasks);
+    const int c = static_cast<int>(task - static_cast<long long>(r) * a.row_tasks);
+    const int len = a.ctx[r];
+    const int live = len <= 0 ? 0 : min((len + PKV_BLOCK_TOKENS - 1) / PKV_BLOCK_TOKENS, a.row_entries);
+    if (live == 0) return;
+    const size_t byte_lo = a.tab_byte0 + static_cast<size_t>(r) * a.row_entries * 4;
+    const size_t w_lo = byte_lo / 16 + static_cast<size_t>(c) * kStageRowWords;  // this task's first word
+    const size_t w_end = (byte_lo + static_cast<size_t>(live) * 4 + 15) / 16;     // past the row's last live word
+    if (w_lo >= w_end) return;
+    size_t w[kStageUnroll];
+    uint4 v[kStageUnroll];
+#pragma unroll
+    for (int u = 0; u < kStageUnroll; ++u) {
+        w[u] = w_lo + u * 32 + lane;
+        if (w[u] < w_end) v[u] = a.src[w[u]];
+    }
+#pragma unroll
+    for (int u = 0; u < kStageUnroll; ++u)
+        if (w[u] < w_end) a.dst[w[u]] = v[u];
 }
 
 }  // namespace attn
@@ -526,11 +574,25 @@ pkv_status pkv_decode_step_host(const void* host_packed, void* device_staging, i
     cudaStream_t s = as_stream(stream);
     cudaError_t e = cudaSuccess;
     if (src) {
-        const size_t n16 = lay.bytes / 16;  // lay.bytes is a multiple of 256
+        attn::StageArgs a;
+        a.src = static_cast<const uint4*>(src);
+        a.dst = static_cast<uint4*>(device_staging);
+        a.n16 = lay.bytes / 16;  // lay.bytes and every field offset are multiples of 256
+        a.tab_lo = lay.block_tables / 16;
+        a.tab_hi = lay.context_lens / 16;  // the table region, with its padding to 256 bytes
+        a.tab_byte0 = lay.block_tables;
+        a.ctx = reinterpret_cast<const int32_t*>(static_cast<const uint8_t*>(src) + lay.context_lens);
+        a.rows = num_seqs;
+        a.row_entries = max_blocks_per_seq;
+        // a row's words can start mid-word: one word more than its length
+        a.row_tasks = static_cast<int>((static_cast<size_t>(max_blocks_per_seq) * 4 / 16 + 1 + attn::kStageRowWords - 1) /
+                                       attn::kStageRowWords);
         const size_t per_block = static_cast<size_t>(attn::kStageThreads) * attn::kStageUnroll;
-        const unsigned grid = static_cast<unsigned>(std::min<size_t>((n16 + per_block - 1) / per_block, 4096));
-        attn::stage_kernel<<<grid, attn::kStageThreads, 0, s>>>(static_cast<const uint4*>(src),
-                                                                static_cast<uint4*>(device_staging), n16);
+        const size_t dense = a.n16 - (a.tab_hi - a.tab_lo);
+        a.dense_blocks = static_cast<int>(std::max<size_t>(1, std::min<size_t>((dense + per_block - 1) / per_block, 4096)));
+        const size_t tasks = static_cast<size_t>(a.rows) * a.row_tasks;
+        const size_t task_blocks = (tasks + attn::kStageThreads / 32 - 1) / (attn::kStageThreads / 32);
+        attn::stage_kernel<<<static_cast<unsigned>(a.dense_blocks + task_blocks), attn::kStageThreads, 0, s>>>(a);
         e = cudaGetLastError();
     } else {
         e = cudaMemcpyAsync(device_staging, host_packed, lay.bytes, cudaMemcpyHostToDevice, s);

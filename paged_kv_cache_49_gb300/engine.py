@@ -278,6 +278,19 @@ class HostStep:
         return nat.step_layout(self.num_seqs, self.eng.num_q_heads, self.eng.num_kv_heads, self.eng.head_dim,
                                self.width, n)["bytes"]
 
+    def h2d_bytes(self) -> int:
+        """Bytes the staging kernel brings across the host link for the packed
+        step: every field but the block tables whole, and of each table row
+        the 16-byte words holding its entries up to ceil(context_len / 16)."""
+        lay = nat.step_layout(self.num_seqs, self.eng.num_q_heads, self.eng.num_kv_heads, self.eng.head_dim,
+                              self.width, self.num_pairs)
+        dense = lay["bytes"] - (lay["context_lens"] - lay["block_tables"])
+        ctx = self.field("context_lens").numpy().astype(np.int64)
+        live = np.minimum(np.maximum((ctx + nat.BLOCK_TOKENS - 1) // nat.BLOCK_TOKENS, 0), self.width)
+        start = lay["block_tables"] + np.arange(self.num_seqs, dtype=np.int64) * self.width * 4
+        words = np.where(live > 0, (start + live * 4 + 15) // 16 - start // 16, 0)
+        return int(dense + 16 * words.sum())
+
     def run(self, scale: float, num_ctas: int = 0, stream=None) -> torch.Tensor:
         """Enqueue the step; out_host holds the output once the stream passes it."""
         e = self.eng

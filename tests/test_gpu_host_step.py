@@ -112,3 +112,39 @@ def test_host_step_inputs_from_pageable_memory(pkv):
         pools.append((eng.k_cache.clone(), eng.v_cache.clone()))
     for o, (kc, vc) in zip(outs[1:], pools[1:]):
         assert torch.equal(o, outs[0]) and torch.equal(kc, pools[0][0]) and torch.equal(vc, pools[0][1])
+
+
+def test_host_step_stages_only_live_table_entries(pkv):
+    """The staging kernel brings every field of the packed inputs but the
+    block tables whole, and of each table row only the 16-byte words that
+    hold its entries up to ceil(context_len / 16); the rest of each row in
+    the device buffer keeps what it held. Rows of 13 entries (52 bytes) start
+    mid-word; one row has no context."""
+    w = make_workload("tiny")
+    q, k, v = w.step_inputs()
+    host = _engine(pkv, w)
+    slots, pairs = host.bm.prepare_append(w.batch)
+    width = 13
+    tables, ctx = host.bm.batch_tables(w.batch, width)
+    ctx[1] = 0  # a row with no context: none of its entries cross
+    step = pkv.HostStep(host, len(w.batch), width, max_pairs=len(w.batch))
+    step.pack(pkv.bf16_from_bits(q), pkv.bf16_from_bits(k), pkv.bf16_from_bits(v), slots, tables, ctx, pairs)
+    step.staging.fill_(0xA5)
+    step.run(w.scale)
+    torch.cuda.synchronize()
+    assert host.read_errors() == 0 and step.workspace.read_error() == 0
+    dev = step.staging.cpu().numpy()
+    src = step.host.numpy()
+    # the layout for this step's pairs (the buffers are sized for max_pairs)
+    lay = pkv.step_layout(len(w.batch), w.num_q_heads, w.num_kv_heads, w.head_dim, width, step.num_pairs)
+    t0, t1, end = lay["block_tables"], lay["context_lens"], lay["bytes"]
+    assert np.array_equal(dev[:t0], src[:t0]) and np.array_equal(dev[t1:end], src[t1:end])
+    copied = np.zeros(t1 - t0, dtype=bool)
+    for r, c in enumerate(ctx.tolist()):
+        live = min(max((c + 15) // 16, 0), width)
+        a = t0 + r * width * 4
+        if live:
+            copied[(a // 16) * 16 - t0: ((a + live * 4 + 15) // 16) * 16 - t0] = True
+        assert np.array_equal(dev[a: a + live * 4], src[a: a + live * 4])
+    assert (dev[t0:t1][~copied] == 0xA5).all()  # nothing else of the tables crossed
+    assert step.h2d_bytes() == (lay["bytes"] - (t1 - t0)) + int(copied.sum())
