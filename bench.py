@@ -118,6 +118,13 @@ def unique_kv_bytes(tables, ctx, hkv, d=128, block_tokens=16):
     return len(used) * hkv * block_tokens * d * 2 * 2
 
 
+def tail_waste_tokens(ctx, block_tokens=16):
+    """Slots of the batch's last blocks that hold no token: a sequence of n
+    tokens occupies ceil(n / b) blocks, wasting b * ceil(n / b) - n slots."""
+    ctx = np.asarray(ctx, dtype=np.int64)
+    return int((((ctx + block_tokens - 1) // block_tokens) * block_tokens - ctx)[ctx > 0].sum())
+
+
 def measured_peak_gbs():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -500,6 +507,8 @@ def measure(pkv, name, args, rank, world, local, flush, e2e_on=True):
     ctx = sb.ctx.cpu().numpy()
     B = w.batch_size
     stream = torch.cuda.current_stream()
+    pool = dict(eng.bm.stats(), num_blocks=w.pool_blocks,
+                tail_waste_tokens=tail_waste_tokens(ctx, w.block_tokens))  # the block manager's counters
 
     for _ in range(args.warmup):
         eng.run_step(sb, w.scale, args.num_ctas)
@@ -653,7 +662,7 @@ def measure(pkv, name, args, rank, world, local, flush, e2e_on=True):
             "tensor_core_speedup": fma_s / attn_s}
     res = {
         "w": w, "value": whole_job_rate(B, world, ms), "ms_per_step": ms, "e2e": e2e, "gpu_launches": launches,
-        "roofline": roofline, "clocks": clk.summary(),
+        "roofline": roofline, "clocks": clk.summary(), "pool": pool,
         "timing_ms": {"step": stats_of(ev_step), "attention_alone": stats_of(ev_attn),
                       "append_alone": stats_of(ev_app), "block_copy_alone": stats_of(ev_copy),
                       "attention_cascade": stats_of(ev_cas), "attention_cuda_cores": stats_of(ev_fma)},
@@ -700,7 +709,7 @@ def run_ours(args):
             torch.cuda.empty_cache()  # the previous workload's pool
             m = measure(pkv, name, args, rank, world, local, flush, e2e_on=not args.no_e2e)
             others[name] = {k: m[k] for k in ("value", "ms_per_step", "e2e", "roofline", "timing_ms", "clocks",
-                                              "config", "gpu_launches")}
+                                              "config", "gpu_launches", "pool")}
         cpu = time_oracle(pool, args.cpu_seconds, head["w"]) if pool is not None and rank == 0 else None
     finally:
         if pool is not None:
@@ -715,7 +724,7 @@ def run_ours(args):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": head["config"],
         "clocks": head["clocks"], "e2e": head["e2e"],
         "gpu_launches": head["gpu_launches"] + sum(o["gpu_launches"] for o in others.values()),
-        "roofline": head["roofline"], "timing_ms": head["timing_ms"], "cpu_baseline": cpu,
+        "roofline": head["roofline"], "timing_ms": head["timing_ms"], "pool": head["pool"], "cpu_baseline": cpu,
         "per_workload": others,
     }
     print(json.dumps(line), flush=True)

@@ -90,3 +90,9 @@ def test_oracle_cores_equal_the_single_process_oracle():
             assert all(np.array_equal(out2[r], out[r]) for r in rows)
         finally:
             pool.close()
+
+
+def test_tail_waste_counts_the_empty_slots_of_last_blocks():
+    # 1 -> 15 empty slots, 16 -> 0, 17 -> 15, 203 -> 5, 0 -> no block
+    assert bench.tail_waste_tokens([1, 16, 17, 203, 0]) == 15 + 0 + 15 + 5
+    assert bench.tail_waste_tokens([8, 9], block_tokens=8) == 0 + 7
