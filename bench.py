@@ -330,7 +330,7 @@ def time_oracle(pool, min_seconds, w):
         busy.append(b)
     n = len(pool.rows)
     return {"value": n * len(walls) / sum(walls), "unit": UNIT, "cores": pool.workers, "kind": "oracle",
-            "sample": pool.describe(w) + f"; {len(walls)} timed passes, {sum(walls):.1f} s",
+            "sample": pool.describe(w), "timing": f"{len(walls)} timed passes over the sample, {sum(walls):.1f} s",
             "single_core_value": n * len(busy) / sum(busy),
             "single_core_note": "the same passes' summed per-process busy time (the time one core would take)"}
 
@@ -367,7 +367,7 @@ def run_reference(args):
                    "kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_tokens": 16,
                    "sample_sequences": len(rows), "sample_context_tokens": pool.context_tokens},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": pool.workers, "kind": "oracle",
-                         "sample": pool.describe(w) + "; one pass over the sample per step",
+                         "sample": pool.describe(w), "timing": "one pass over the sample per step",
                          "single_core_value": len(rows) * args.steps / sum(busy)},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
