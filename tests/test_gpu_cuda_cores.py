@@ -88,3 +88,40 @@ def test_cuda_core_variant_refuses_other_group_sizes(pkv):
     with pytest.raises(pkv.PkvError) as e:
         pkv.attn_decode_cuda_cores(sb.q, eng.k_cache, eng.v_cache, sb.tables, sb.ctx, w.scale)
     assert e.value.status == -6  # PKV_EUNSUPPORTED
+
+
+@pytest.mark.parametrize("hq", [8, 16])
+def test_cuda_core_variant_at_a_large_batch(pkv, hq):
+    """3,000 sequences: the one-merge-slot instantiations of the variant
+    (group sizes 4 and 8), empty contexts included, on a sample of rows."""
+    from oracle import paged_attention as pa
+    from workloads import randn_bf16
+
+    rng = np.random.default_rng(50 + hq)
+    B, hkv, d, bt = 3000, 2, 128, 16
+    ctx = rng.integers(1, 90, size=B).astype(np.int32)
+    ctx[::101] = 0
+    nblk = -(-ctx // bt)
+    width = int(nblk.max())
+    nb = int(nblk.sum()) + 4
+    perm = rng.permutation(nb).astype(np.int32)
+    tables = np.full((B, width), -1, np.int32)
+    nxt = 0
+    for s in range(B):
+        tables[s, :nblk[s]] = perm[nxt:nxt + nblk[s]]
+        nxt += int(nblk[s])
+    kp, vp = randn_bf16(rng, (nb, hkv, bt, d)), randn_bf16(rng, (nb, hkv, bt, d))
+    q = randn_bf16(rng, (B, hq, d))
+    dev = torch.device("cuda")
+    t = lambda bits: pkv.bf16_from_bits(bits).to(dev)
+    scale = d ** -0.5
+    rows = sorted(set(range(0, B, 11)) | set(range(0, B, 101)) | {B - 1})
+    ref = pa.paged_decode_attention(q, kp, vp, tables, ctx, scale, seqs=rows)
+    ws = pkv.AttentionWorkspace(B, hkv)
+    out = torch.full((B, hq, d), float("nan"), dtype=torch.bfloat16, device=dev)
+    pkv.attn_decode_cuda_cores(t(q), t(kp), t(vp), torch.from_numpy(tables).to(dev), torch.from_numpy(ctx).to(dev),
+                               scale, out, ws)
+    torch.cuda.synchronize()
+    assert ws.read_error() == 0
+    assert (out[::101] == 0).all().item()  # empty contexts give zero rows
+    _close(out, ref[rows], rows)
