@@ -188,48 +188,53 @@ __device__ __forceinline__ int run_blocks(const int* scan, int s) {
     return scan[s] - (s > 0 ? scan[s - 1] : 0);
 }
 
-// Smallest s with scan[s] > t (scan is the inclusive prefix of run lengths).
-__device__ __forceinline__ int find_seq(const int* scan, int n, int t) {
-    int lo = 0, hi = n - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (scan[mid] > t) hi = mid; else lo = mid + 1;
+// Smallest i in [0, n) for which pred(i) holds, for a predicate that is
+// false below some index and true from there on, and true at n - 1. The whole
+// warp calls it. Each round splits the interval into 32 chunks, one per lane,
+// and keeps the first chunk whose last index satisfies the predicate: 64
+// sequences take two rounds of one shared-memory read per lane, where a
+// binary search takes six dependent reads (about 100 cycles each on the
+// start-up path, where every step is serial).
+template <class Pred>
+__device__ __forceinline__ int warp_first_true(int n, Pred pred) {
+    const int lane = static_cast<int>(threadIdx.x & 31);
+    int lo = 0, len = n;
+    while (len > 1) {
+        const int step = (len + 31) >> 5;
+        const int i = min(lo + (lane + 1) * step, lo + len) - 1;
+        const int c = __ffs(__ballot_sync(0xffffffffu, pred(i))) - 1;
+        lo += c * step;
+        len = min(step, len - c * step);
     }
     return lo;
 }
 
+// a / b for 0 <= a < 2^30 and b >= 1 whose quotient is small (below the KV
+// head count where it is used): a single-precision estimate, then corrected
+// to the exact quotient. Shorter than an integer division on the start-up
+// path, where only one thread needs it.
+__device__ __forceinline__ int div_small(int a, int b) {
+    int q = static_cast<int>(__fdividef(static_cast<float>(a), static_cast<float>(b)));
+    while (q > 0 && q * b > a) --q;
+    while ((q + 1) * b <= a) ++q;
+    return q;
+}
+
+// Position x of the line (x < total) as a cursor. The whole warp calls it.
 // Positions on the line, and cost positions of the work partition, are
 // 32-bit: the host rejects launches whose line could reach 2^30 cost units.
 __device__ __forceinline__ Cursor locate(const int* scan, int n, int hkv, int x) {
     Cursor c;
-    c.s = find_seq(scan, n, x / hkv);
+    // the sequence: smallest s with hkv * scan[s] > x, i.e. scan[s] > floor(x / hkv)
+    c.s = warp_first_true(n, [&](int i) { return hkv * scan[i] > x; });
     const int nb = run_blocks(scan, c.s);
-    const int off = x - hkv * (scan[c.s] - nb);
-    c.g = off / nb;
+    const int off = x - hkv * (scan[c.s] - nb);  // in [0, hkv * nb)
+    // the run, off / nb: lanes 1 .. hkv - 1 count the run starts at or below
+    // off (a division beyond 32 KV heads)
+    const int lane = static_cast<int>(threadIdx.x & 31);
+    c.g = hkv <= 32 ? __popc(__ballot_sync(0xffffffffu, lane >= 1 && lane < hkv && lane * nb <= off)) : off / nb;
     c.blk = off - c.g * nb;
     return c;
-}
-
-// The work partition deals out cost, not tiles: tile x of run r = s * hkv + g
-// sits at cost position x + kPieceCost * r, so that each run is followed by a
-// gap of kPieceCost positions that hold no tile. Sequence s's runs start at
-// cost hkv * (scan[s-1] + kPieceCost * s), each run taking nb + kPieceCost
-// positions. Returns the first tile whose cost position is >= y (total when
-// none is).
-__device__ __forceinline__ int line_at(const int* scan, int n, int hkv, int y, int total, int cost_total) {
-    if (y >= cost_total) return total;
-    const int t = y / hkv;
-    int lo = 0, hi = n - 1;  // smallest s with scan[s] + kPieceCost * (s + 1) > t
-    while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (scan[mid] + kPieceCost * (mid + 1) > t) hi = mid; else lo = mid + 1;
-    }
-    const int nb = run_blocks(scan, lo);
-    const int before = scan[lo] - nb;  // tiles of one head before sequence lo
-    const int off = y - hkv * (before + kPieceCost * lo);
-    const int g = off / (nb + kPieceCost);
-    const int w = off - g * (nb + kPieceCost);
-    return hkv * before + g * nb + min(w, nb);
 }
 
 __device__ __forceinline__ void advance(Cursor& c, const int* scan, int n, int hkv, int len) {
@@ -241,11 +246,6 @@ __device__ __forceinline__ void advance(Cursor& c, const int* scan, int n, int h
             do { ++c.s; } while (c.s < n && run_blocks(scan, c.s) == 0);
         }
     }
-}
-
-__device__ __forceinline__ int clamped_ctx(const Params& p, int s) {
-    const int c = __ldg(p.context_lens + s);
-    return c > p.cap_tokens ? p.cap_tokens : c;
 }
 
 // One piece: blocks [blk, blk + len) of the run of (sequence s, KV head g),
@@ -577,6 +577,17 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     }
 
     // ---- plan: inclusive prefix sum of block-run lengths over sequences ----
+    // The work partition deals out cost, not tiles: tile x of run r = s * hkv
+    // + g sits at cost position x + kPieceCost * r, so that each run is
+    // followed by a gap of kPieceCost positions that hold no tile. CTA b takes
+    // the tiles whose cost position lies in [b, b + 1) * cchunk: equal shares
+    // of tiles plus per-run overhead, so that a CTA whose range is cut into
+    // many short pieces streams fewer tiles. Each end of that range is found
+    // by the thread holding the sequence whose cost span contains it, while
+    // it writes the prefix sum: no search of the prefix sum and no third
+    // block barrier stand between the context lengths and the first copy.
+    int* ends = misc + 2;  // misc[2], misc[3]: the CTA's range [lo, hi) of tiles
+    int cchunk;
     {
         const int per = (B + kThreads - 1) / kThreads;
         const int lo = min(B, tid * per);
@@ -597,6 +608,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 }
                 skip[s] = sk;
             }
+            scan[s] = all - sk;  // the run length; the second pass turns it into the prefix
+            tail[s] = static_cast<uint8_t>(cc - kTok * (all - 1));  // 1..16 (unused when all == 0)
             local += all - sk;
         }
         int v = local;
@@ -607,26 +620,43 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         }
         if (lane == 31) warp_tot[warp] = v;
         __syncthreads();
-        int run = v - local;
-        for (int w = 0; w < warp; ++w) run += warp_tot[w];
+        int run = v - local, per_head = 0;
+#pragma unroll
+        for (int w = 0; w < kThreads / 32; ++w) {
+            const int t = warp_tot[w];
+            per_head += t;
+            if (w < warp) run += t;
+        }
+        const int cost_total = Hkv * (per_head + kPieceCost * B);
+        cchunk = (cost_total + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
+        const int y_lo = static_cast<int>(blockIdx.x) * cchunk;
+        const int y_hi = y_lo + cchunk;
         for (int s = lo; s < hi; ++s) {
-            const int cc = clamped_ctx(p, s);
-            const int tiles = cc > 0 ? (cc + kTok - 1) / kTok : 0;
-            run += tiles - (skip ? skip[s] : 0);
+            const int before = run;
+            run += scan[s];
             scan[s] = run;
-            tail[s] = static_cast<uint8_t>(cc - kTok * (tiles - 1));  // 1..16 (unused when tiles == 0)
+            // Sequence s spans cost positions [c0, c0 + hkv * (nb + kPieceCost)):
+            // run g's tiles at c0 + g * (nb + kPieceCost) + j for j < nb, then
+            // its gap. The range end at y is the first tile at or after y.
+            const int nb = run - before;
+            const int c0 = Hkv * (before + kPieceCost * s);
+            const int c1 = c0 + Hkv * (nb + kPieceCost);
+            auto tile_at = [&](int y) {
+                const int off = y - c0;
+                const int g = div_small(off, nb + kPieceCost);
+                return Hkv * before + g * nb + min(off - g * (nb + kPieceCost), nb);
+            };
+            if (y_lo >= c0 && y_lo < c1) ends[0] = tile_at(y_lo);
+            if (y_hi >= c0 && y_hi < c1) ends[1] = tile_at(y_hi);
+        }
+        if (tid == 0) {  // an end past the last cost position: the line's end
+            if (y_lo >= cost_total) ends[0] = Hkv * per_head;
+            if (y_hi >= cost_total) ends[1] = Hkv * per_head;
         }
         __syncthreads();
     }
-
-    // CTA b takes the tiles whose cost position lies in [b, b + 1) * cchunk:
-    // equal shares of tiles plus per-run overhead, so that a CTA whose range
-    // is cut into many short pieces streams fewer tiles.
-    const int total = Hkv * scan[B - 1];
-    const int cost_total = Hkv * (scan[B - 1] + kPieceCost * B);
-    const int cchunk = (cost_total + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
-    const int range_lo = line_at(scan, B, Hkv, static_cast<int>(blockIdx.x) * cchunk, total, cost_total);
-    const int range_hi = line_at(scan, B, Hkv, static_cast<int>(blockIdx.x + 1) * cchunk, total, cost_total);
+    const int range_lo = ends[0];
+    const int range_hi = ends[1];
 
     // The merge warp, idle until the first piece ends, warms L2 with the
     // block-table entries and query rows of this CTA's range -- two
