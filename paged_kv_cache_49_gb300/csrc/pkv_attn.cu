@@ -40,19 +40,33 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// 2-D view of a cache: rows = num_blocks * Hkv * block_tokens token rows of
-// 128 bf16; a box is 64 columns by min(16, block_tokens) rows.
+// View of a cache as token rows (num_blocks * Hkv * block_tokens rows of 128
+// bf16). Blocks of 16 tokens or more: 3-D, {64 columns, rows, 2 column
+// halves} with the halves 128 bytes apart, so that one box of {64, 16, 2}
+// brings 16 rows of one (block, KV head) -- 4 KB -- laid out in shared memory
+// as the two 16 x 64 halves one after the other, each in the 128-byte
+// swizzle. 8-token blocks: 2-D, {64 columns, rows}, boxes of 64 x 8 (a tile
+// takes two blocks).
 bool make_cache_map(CUtensorMap* map, const void* base, int num_blocks, int hkv, int block_tokens) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(kDim),
-                          static_cast<cuuint64_t>(num_blocks) * hkv * block_tokens};
+    const cuuint64_t rows = static_cast<cuuint64_t>(num_blocks) * hkv * block_tokens;
+    if (block_tokens >= kTok) {
+        cuuint64_t dims[3] = {64, rows, 2};
+        cuuint64_t strides[2] = {static_cast<cuuint64_t>(kDim) * 2, 128};
+        cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kTok), 2};
+        cuuint32_t estr[3] = {1, 1, 1};
+        return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    }
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(kDim), rows};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(kDim) * 2};
-    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(block_tokens < kTok ? block_tokens : kTok)};
+    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(block_tokens)};
     cuuint32_t estr[2] = {1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 using KernelFn = void (*)(CUtensorMap, CUtensorMap, Params);
@@ -237,6 +251,7 @@ pkv_status prepare(const void* q, const void* k_cache, const void* v_cache, cons
     prm.skip_tiles = nullptr;
     prm.side = nullptr;
     prm.stop_tiles = -1;
+    prm.early_issue = 0;
     L->grid = grid;
     L->slots = kc.slots;
     L->fn = kc.fn;
@@ -245,7 +260,9 @@ pkv_status prepare(const void* q, const void* k_cache, const void* v_cache, cons
 }
 
 // early: launch with programmatic stream serialization, so that the kernel's
-// prologue overlaps the previous kernel on the stream (see griddep_wait).
+// prologue overlaps the previous kernel on the stream (see griddep_wait);
+// its first tile copies then wait for that kernel. Otherwise they may go out
+// during the plan.
 pkv_status launch(const Launch& L, cudaStream_t stream, bool early) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(L.grid);
@@ -257,7 +274,9 @@ pkv_status launch(const Launch& L, cudaStream_t stream, bool early) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = early ? 1 : 0;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, L.fn, L.tm_k, L.tm_v, L.prm);
+    Params prm = L.prm;
+    prm.early_issue = early ? 0 : 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, L.fn, L.tm_k, L.tm_v, prm);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) {
         record_cuda_error(e);
@@ -715,10 +734,8 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                         const uint32_t fb = full_bar(stage);
                         mbar_arrive_expect_tx(fb, kStageBytes);
                         const uint32_t dst = smem_u32(smem + stage * kStageBytes);
-                        tma_load_2d(dst, &tm_k, 0, ya, fb, policy);
-                        tma_load_2d(dst + kHalfBytes, &tm_k, 64, ya, fb, policy);
-                        tma_load_2d(dst + kBlockBytes, &tm_v, 0, ya, fb, policy);
-                        tma_load_2d(dst + kBlockBytes + kHalfBytes, &tm_v, 64, ya, fb, policy);
+                        tma_load_3d(dst, &tm_k, 0, ya, 0, fb, policy);
+                        tma_load_3d(dst + kBlockBytes, &tm_v, 0, ya, 0, fb, policy);
                         ++issued;
                     }
                     if (++stage == kPfxStages) { stage = 0; sphase ^= 1u; }
@@ -1337,6 +1354,7 @@ extern "C" pkv_status pkv_attn_decode_static(const void* q, const void* k_cache,
     prm.skip_tiles = nullptr;
     prm.side = nullptr;
     prm.stop_tiles = -1;
+    prm.early_issue = 1;  // an ordinary launch: stream order covers earlier writes
 
     void* args[] = {&tm_k, &tm_v, &prm};
     e = cudaLaunchKernel(reinterpret_cast<const void*>(kc.fn), dim3(grid), dim3(attn::kThreads), args, kc.smem,

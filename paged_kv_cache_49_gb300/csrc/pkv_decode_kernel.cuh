@@ -177,6 +177,10 @@ struct Params {
     // issues the copies of its first stop_tiles tiles and skips the rest, so
     // that a consumer's wait on the next one runs out.
     int stop_tiles;
+    // 1: the first piece's copies may be issued during the plan (the kernel
+    // was not launched behind kernels that write the KV cache); 0: only
+    // after griddep_wait, by the producer.
+    int early_issue;
 };
 
 // Position in the line of (sequence, KV head) block runs.
@@ -523,6 +527,29 @@ __device__ __forceinline__ void fma_consumer_warp(const Params& p, uint8_t* smem
 // plain kernel carries none of its branches. kSlots: merge slots (1 or 2).
 // kFmaG: 0 for the tensor-core consumers; 4 or 8 for the CUDA-core variant
 // of their math compiled for that group size (16-token blocks only).
+// One tile's copies into a stage: K then V, 16 token rows each as one box
+// of both 64-column halves (blocks of 16 tokens or more), or, with 8-token
+// blocks, as 16 x 64 halves whose rows 0-7 come from the block at ya and rows
+// 8-15 from the block at yb.
+template <int kBT>
+__device__ __forceinline__ void issue_tile(uint32_t dst, const CUtensorMap* tm_k, const CUtensorMap* tm_v, int ya,
+                                           int yb, uint32_t fb, uint64_t policy) {
+    if constexpr (kBT >= kTok) {
+        tma_load_3d(dst, tm_k, 0, ya, 0, fb, policy);
+        tma_load_3d(dst + kBlockBytes, tm_v, 0, ya, 0, fb, policy);
+    } else {
+        constexpr uint32_t kRow8 = 8 * 128;
+        tma_load_2d(dst, tm_k, 0, ya, fb, policy);
+        tma_load_2d(dst + kRow8, tm_k, 0, yb, fb, policy);
+        tma_load_2d(dst + kHalfBytes, tm_k, 64, ya, fb, policy);
+        tma_load_2d(dst + kHalfBytes + kRow8, tm_k, 64, yb, fb, policy);
+        tma_load_2d(dst + kBlockBytes, tm_v, 0, ya, fb, policy);
+        tma_load_2d(dst + kBlockBytes + kRow8, tm_v, 0, yb, fb, policy);
+        tma_load_2d(dst + kBlockBytes + kHalfBytes, tm_v, 64, ya, fb, policy);
+        tma_load_2d(dst + kBlockBytes + kHalfBytes + kRow8, tm_v, 64, yb, fb, policy);
+    }
+}
+
 template <int kBT, bool kSkip, int kSlots, int kFmaG = 0>
 __global__ void __launch_bounds__(kThreads, 2)
 decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -573,6 +600,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             mbar_init(mempty_bar(i), 32);
         }
         misc[0] = 0;
+        misc[4] = 0;  // first-piece tiles copied during the plan
+        misc[5] = 0;  // 1: the first piece's query rows too
         fence_barrier_init();
     }
 
@@ -647,7 +676,82 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 return Hkv * before + g * nb + min(off - g * (nb + kPieceCost), nb);
             };
             if (y_lo >= c0 && y_lo < c1) ends[0] = tile_at(y_lo);
-            if (y_hi >= c0 && y_hi < c1) ends[1] = tile_at(y_hi);
+            if (y_hi >= c0 && y_hi < c1) {
+                const int off = y_hi - c0;
+                const int g = div_small(off, nb + kPieceCost);
+                const int r = min(off - g * (nb + kPieceCost), nb);  // tiles of run g before the end
+                const int hi_t = Hkv * before + g * nb + r;
+                ends[1] = hi_t;
+                // The walk's first piece is the part of the range in the run
+                // holding tile hi_t - 1 (run g, or the last tile of run g - 1).
+                // When that run is this sequence's, this thread copies the
+                // piece's first tiles and query rows now, into stages 0.. and
+                // query slot 0, while the rest of the CTA finishes the plan:
+                // the producer's own first copies come several microseconds
+                // after the plan, most of it cold instruction fetch.
+                if (p.early_issue && nb > 0 && (r > 0 || g > 0)) {
+                    const int gl = r > 0 ? g : g - 1;
+                    const int seg = Hkv * before + gl * nb;  // the run's first tile
+                    const int split = y_lo >= c0 ? max(seg, tile_at(y_lo)) : seg;
+                    const int len = hi_t - split;
+                    int n = min(len, kStages);
+                    if (blockIdx.x == 0 && p.stop_tiles >= 0) n = min(n, p.stop_tiles);
+                    if (n > 0) {
+                        const uint64_t policy = policy_evict_first();
+                        if (len >= kConsumerWarps) {
+                            mbar_arrive_expect_tx(qfull_bar(0), G * kDim * 2);
+                            bulk_load(smem_u32(smem + kOffQ),
+                                      p.q + (static_cast<size_t>(s) * p.num_q_heads + static_cast<size_t>(gl) * G) * kDim,
+                                      G * kDim * 2, qfull_bar(0));
+                            misc[5] = 1;
+                        }
+                        const int32_t* row = p.block_tables + static_cast<size_t>(s) * p.max_blocks;
+                        const int sk0 = skip ? skip[s] : 0;
+                        const int t0 = sk0 + (split - seg);  // the first tile's index within the sequence
+                        const int seq_blocks = (kTok * (sk0 + nb - 1) + tail[s] + kBT - 1) / kBT;
+                        auto checked = [&](int bid) {
+                            if (bid < 0 || bid >= p.num_blocks) {
+                                if (p.err) atomicOr(p.err, PKV_DEVERR_BLOCK_ID);
+                                bid = 0;
+                            }
+                            return bid;
+                        };
+                        int e0[kStages], e1[kStages];  // all reads first, then the checks and copies
+#pragma unroll
+                        for (int j = 0; j < kStages; ++j) {
+                            e0[j] = e1[j] = 0;
+                            if (j < n) {
+                                const int t = t0 + j;
+                                if constexpr (kBT >= kTok) {
+                                    e0[j] = __ldg(row + t / (kBT / kTok));
+                                } else {
+                                    e0[j] = __ldg(row + 2 * t);
+                                    if (2 * t + 1 < seq_blocks) e1[j] = __ldg(row + 2 * t + 1);
+                                }
+                            }
+                        }
+#pragma unroll
+                        for (int j = 0; j < kStages; ++j) {
+                            if (j < n) {
+                                const int t = t0 + j;
+                                int ya, yb = 0;
+                                if constexpr (kBT >= kTok) {
+                                    ya = (checked(e0[j]) * Hkv + gl) * kBT + (t % (kBT / kTok)) * kTok;
+                                } else {
+                                    const int b0 = checked(e0[j]);
+                                    const int b1 = 2 * t + 1 < seq_blocks ? checked(e1[j]) : b0;
+                                    ya = (b0 * Hkv + gl) * kBT;
+                                    yb = (b1 * Hkv + gl) * kBT;
+                                }
+                                mbar_arrive_expect_tx(full_bar(j), kStageBytes);
+                                issue_tile<kBT>(smem_u32(smem + kOffStages + j * kStageBytes), &tm_k, &tm_v, ya, yb,
+                                                full_bar(j), policy);
+                            }
+                        }
+                        misc[4] = n;
+                    }
+                }
+            }
         }
         if (tid == 0) {  // an end past the last cost position: the line's end
             if (y_lo >= cost_total) ends[0] = Hkv * per_head;
@@ -716,12 +820,19 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         int tile = 0;  // position in the CTA's stream of tiles
         const int stop_at = (p.stop_tiles >= 0 && blockIdx.x == 0) ? p.stop_tiles : INT_MAX;
         int issued = 0, q_issued = 0;  // copies issued into the stage ring and the query ring
+        // Tiles [0, n_early) and, if q_early, the first query rows were
+        // copied during the plan: skipped here, counted in the drain.
+        const int n_early = misc[4];
+        bool q_early = misc[5] != 0;
         bool waited = false;  // griddep_wait done by this thread
         while (walk.next(pc)) {
             const int len = pc.len;
             if (len >= kConsumerWarps) {  // short pieces: the consumers read their query rows themselves
                 if (lane == 0) {
-                    if (mbar_wait(qempty_bar(qslot), qphase ^ 1u, abort_flag, p.err)) {
+                    if (q_early) {
+                        q_early = false;
+                        ++q_issued;
+                    } else if (mbar_wait(qempty_bar(qslot), qphase ^ 1u, abort_flag, p.err)) {
                         fence_proxy_async_shared();  // the consumers' reads of the slot, before the copy over it
                         mbar_arrive_expect_tx(qfull_bar(qslot), G * kDim * 2);
                         const __nv_bfloat16* src =
@@ -765,27 +876,13 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                             griddep_wait();
                             waited = true;
                         }
-                        // (tests of the bounded waits: past stop_at nothing is issued)
-                        if (tile < stop_at && mbar_wait(empty_bar(stage), sphase ^ 1u, abort_flag, p.err)) {
+                        // tiles in [n_early, stop_at) only (stop_at: tests of the bounded waits)
+                        if (static_cast<unsigned>(tile - n_early) < static_cast<unsigned>(stop_at - n_early) &&
+                            mbar_wait(empty_bar(stage), sphase ^ 1u, abort_flag, p.err)) {
                             const uint32_t fb = full_bar(stage);
                             mbar_arrive_expect_tx(fb, kStageBytes);
-                            const uint32_t dst = smem_u32(smem + kOffStages + stage * kStageBytes);
-                            if constexpr (kBT >= kTok) {
-                                tma_load_2d(dst, &tm_k, 0, ya, fb, policy);
-                                tma_load_2d(dst + kHalfBytes, &tm_k, 64, ya, fb, policy);
-                                tma_load_2d(dst + kBlockBytes, &tm_v, 0, ya, fb, policy);
-                                tma_load_2d(dst + kBlockBytes + kHalfBytes, &tm_v, 64, ya, fb, policy);
-                            } else {  // 8-row boxes: rows 0-7 from one block, rows 8-15 from the next
-                                constexpr uint32_t kRow8 = 8 * 128;
-                                tma_load_2d(dst, &tm_k, 0, ya, fb, policy);
-                                tma_load_2d(dst + kRow8, &tm_k, 0, yb, fb, policy);
-                                tma_load_2d(dst + kHalfBytes, &tm_k, 64, ya, fb, policy);
-                                tma_load_2d(dst + kHalfBytes + kRow8, &tm_k, 64, yb, fb, policy);
-                                tma_load_2d(dst + kBlockBytes, &tm_v, 0, ya, fb, policy);
-                                tma_load_2d(dst + kBlockBytes + kRow8, &tm_v, 0, yb, fb, policy);
-                                tma_load_2d(dst + kBlockBytes + kHalfBytes, &tm_v, 64, ya, fb, policy);
-                                tma_load_2d(dst + kBlockBytes + kHalfBytes + kRow8, &tm_v, 64, yb, fb, policy);
-                            }
+                            issue_tile<kBT>(smem_u32(smem + kOffStages + stage * kStageBytes), &tm_k, &tm_v, ya, yb, fb,
+                                            policy);
                             ++issued;
                         }
                     }
@@ -811,6 +908,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 }
             }
             volatile int never = 0;
+            issued += n_early;
             for (int i = max(0, issued - kStages); i < issued; ++i)
                 mbar_wait(full_bar(i % kStages), static_cast<uint32_t>((i / kStages) & 1), &never, nullptr);
             for (int i = max(0, q_issued - kQSlots); i < q_issued; ++i)
