@@ -106,8 +106,15 @@ struct Layout {
     static constexpr int kOffBar = kOffL + S * kMergeMLFloats * 4;
     static constexpr int kNumBars = 2 * kStages + 2 * kQSlots + 2 * S;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-    static constexpr int kOffScan = kOffMisc + 64;
+    static constexpr int kOffScan = kOffMisc + 128;
 };
+
+// Slots (ints) of the small shared-memory area misc[]
+constexpr int kMiscAbort = 0;    // the CTA's abort flag
+constexpr int kMiscEnds = 2;     // [2], [3]: the CTA's range [lo, hi) of tiles
+constexpr int kMiscEarly = 4;    // [4]: first-piece tiles copied by the merge warp, [5]: 1 if its query rows too
+constexpr int kMiscWarpTot = 8;  // [8, 8 + warps): per-warp sums of the plan
+constexpr int kMiscFirst = 16;   // [16, 20): the walk's first piece: sequence (or -1), run, block, line position
 
 __host__ __device__ constexpr int off_scan(int slots) {
     return slots == 1 ? Layout<1>::kOffScan : Layout<2>::kOffScan;
@@ -271,15 +278,24 @@ struct PieceWalk {
     int part;
     Cursor c;
 
-    __device__ PieceWalk(const int* scan_, int n_, int hkv_, int lo, int hi)
+    // first: the first piece as the plan found it (sequence, run, block,
+    // line position), or first[0] = -1 when the plan left it to the search.
+    __device__ PieceWalk(const int* scan_, int n_, int hkv_, int lo, int hi, const int* first)
         : scan(scan_), n(n_), hkv(hkv_), range_lo(lo), part(0) {
-        const Cursor last = locate(scan, n, hkv, hi - 1);
-        const int nb = run_blocks(scan, last.s);
-        const int seg = hkv * (scan[last.s] - nb) + last.g * nb;
-        split = seg > lo ? seg : lo;
-        x = split;
         end = hi;
-        c = locate(scan, n, hkv, x);
+        if (first[0] >= 0) {
+            c.s = first[0];
+            c.g = first[1];
+            c.blk = first[2];
+            split = first[3];
+        } else {
+            const Cursor last = locate(scan, n, hkv, hi - 1);
+            const int nb = run_blocks(scan, last.s);
+            const int seg = hkv * (scan[last.s] - nb) + last.g * nb;
+            split = seg > lo ? seg : lo;
+            c = locate(scan, n, hkv, split);
+        }
+        x = split;
     }
 
     __device__ bool next(Piece& pc) {
@@ -332,8 +348,8 @@ __device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
 
 template <int kSlots, int G>
 __device__ __forceinline__ void fma_consumer_warp(const Params& p, uint8_t* smem, const int* scan,
-                                                  const uint8_t* tail, int range_lo, int range_hi, int warp,
-                                                  int lane, volatile int* abort_flag, uint32_t bar0) {
+                                                  const uint8_t* tail, int range_lo, int range_hi, const int* first,
+                                                  int warp, int lane, volatile int* abort_flag, uint32_t bar0) {
     static_assert(G == 4 || G == 8, "CUDA-core variant: group sizes 4 and 8");
     using LY = Layout<kSlots>;
     constexpr int kTpc = 32 / G;         // tokens per reduce-scatter round
@@ -357,7 +373,7 @@ __device__ __forceinline__ void fma_consumer_warp(const Params& p, uint8_t* smem
     const int my_tok = lane / G;
     const float NEG_INF = -INFINITY;
 
-    PieceWalk walk(scan, B, Hkv, range_lo, range_hi);
+    PieceWalk walk(scan, B, Hkv, range_lo, range_hi, first);
     Piece pc;
     int gidx0 = 0, qslot = 0, piece = 0;
     uint32_t qphase = 0;
@@ -569,8 +585,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     int* skip = kSkip ? reinterpret_cast<int*>(smem + skip_offset(B, kSlots)) : nullptr;
     auto skipped = [&](int s) { return skip ? skip[s] : 0; };
     int* misc = reinterpret_cast<int*>(smem + LY::kOffMisc);
-    volatile int* abort_flag = misc;  // misc[0]
-    int* warp_tot = misc + 8;         // misc[8 .. 8 + kThreads / 32)
+    volatile int* abort_flag = misc + kMiscAbort;
+    int* warp_tot = misc + kMiscWarpTot;  // kThreads / 32 of them
+    const int* first = misc + kMiscFirst;
     float* sm_o = reinterpret_cast<float*>(smem + kOffO);
     float* sm_m = reinterpret_cast<float*>(smem + LY::kOffM);
     float* sm_l = reinterpret_cast<float*>(smem + LY::kOffL);
@@ -600,8 +617,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             mbar_init(mempty_bar(i), 32);
         }
         misc[0] = 0;
-        misc[4] = 0;  // first-piece tiles copied during the plan
-        misc[5] = 0;  // 1: the first piece's query rows too
+        misc[kMiscEarly] = 0;
+        misc[kMiscEarly + 1] = 0;
+        misc[kMiscFirst] = -1;
         fence_barrier_init();
     }
 
@@ -615,7 +633,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     // by the thread holding the sequence whose cost span contains it, while
     // it writes the prefix sum: no search of the prefix sum and no third
     // block barrier stand between the context lengths and the first copy.
-    int* ends = misc + 2;  // misc[2], misc[3]: the CTA's range [lo, hi) of tiles
+    int* ends = misc + kMiscEnds;
     int cchunk;
     {
         const int per = (B + kThreads - 1) / kThreads;
@@ -683,72 +701,27 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 const int hi_t = Hkv * before + g * nb + r;
                 ends[1] = hi_t;
                 // The walk's first piece is the part of the range in the run
-                // holding tile hi_t - 1 (run g, or the last tile of run g - 1).
-                // When that run is this sequence's, this thread copies the
-                // piece's first tiles and query rows now, into stages 0.. and
-                // query slot 0, while the rest of the CTA finishes the plan:
-                // the producer's own first copies come several microseconds
-                // after the plan, most of it cold instruction fetch.
-                if (p.early_issue && nb > 0 && (r > 0 || g > 0)) {
+                // holding tile hi_t - 1 (run g, or the last tile of run g -
+                // 1). When that run is this sequence's, this thread records
+                // the piece, so that no warp searches for it, and, when the
+                // kernel may read the cache at once, how many of its tiles the
+                // merge warp (idle until the first piece ends) copies right
+                // after the plan: the producer's own first copies come several
+                // microseconds later, most of it cold instruction fetch.
+                if (nb > 0 && (r > 0 || g > 0)) {
                     const int gl = r > 0 ? g : g - 1;
                     const int seg = Hkv * before + gl * nb;  // the run's first tile
                     const int split = y_lo >= c0 ? max(seg, tile_at(y_lo)) : seg;
                     const int len = hi_t - split;
-                    int n = min(len, kStages);
-                    if (blockIdx.x == 0 && p.stop_tiles >= 0) n = min(n, p.stop_tiles);
-                    if (n > 0) {
-                        const uint64_t policy = policy_evict_first();
-                        if (len >= kConsumerWarps) {
-                            mbar_arrive_expect_tx(qfull_bar(0), G * kDim * 2);
-                            bulk_load(smem_u32(smem + kOffQ),
-                                      p.q + (static_cast<size_t>(s) * p.num_q_heads + static_cast<size_t>(gl) * G) * kDim,
-                                      G * kDim * 2, qfull_bar(0));
-                            misc[5] = 1;
-                        }
-                        const int32_t* row = p.block_tables + static_cast<size_t>(s) * p.max_blocks;
-                        const int sk0 = skip ? skip[s] : 0;
-                        const int t0 = sk0 + (split - seg);  // the first tile's index within the sequence
-                        const int seq_blocks = (kTok * (sk0 + nb - 1) + tail[s] + kBT - 1) / kBT;
-                        auto checked = [&](int bid) {
-                            if (bid < 0 || bid >= p.num_blocks) {
-                                if (p.err) atomicOr(p.err, PKV_DEVERR_BLOCK_ID);
-                                bid = 0;
-                            }
-                            return bid;
-                        };
-                        int e0[kStages], e1[kStages];  // all reads first, then the checks and copies
-#pragma unroll
-                        for (int j = 0; j < kStages; ++j) {
-                            e0[j] = e1[j] = 0;
-                            if (j < n) {
-                                const int t = t0 + j;
-                                if constexpr (kBT >= kTok) {
-                                    e0[j] = __ldg(row + t / (kBT / kTok));
-                                } else {
-                                    e0[j] = __ldg(row + 2 * t);
-                                    if (2 * t + 1 < seq_blocks) e1[j] = __ldg(row + 2 * t + 1);
-                                }
-                            }
-                        }
-#pragma unroll
-                        for (int j = 0; j < kStages; ++j) {
-                            if (j < n) {
-                                const int t = t0 + j;
-                                int ya, yb = 0;
-                                if constexpr (kBT >= kTok) {
-                                    ya = (checked(e0[j]) * Hkv + gl) * kBT + (t % (kBT / kTok)) * kTok;
-                                } else {
-                                    const int b0 = checked(e0[j]);
-                                    const int b1 = 2 * t + 1 < seq_blocks ? checked(e1[j]) : b0;
-                                    ya = (b0 * Hkv + gl) * kBT;
-                                    yb = (b1 * Hkv + gl) * kBT;
-                                }
-                                mbar_arrive_expect_tx(full_bar(j), kStageBytes);
-                                issue_tile<kBT>(smem_u32(smem + kOffStages + j * kStageBytes), &tm_k, &tm_v, ya, yb,
-                                                full_bar(j), policy);
-                            }
-                        }
-                        misc[4] = n;
+                    if (len > 0) {
+                        misc[kMiscFirst] = s;
+                        misc[kMiscFirst + 1] = gl;
+                        misc[kMiscFirst + 2] = split - seg;
+                        misc[kMiscFirst + 3] = split;
+                        int n = p.early_issue ? min(len, kStages) : 0;
+                        if (blockIdx.x == 0 && p.stop_tiles >= 0) n = min(n, p.stop_tiles);
+                        misc[kMiscEarly] = n;
+                        misc[kMiscEarly + 1] = n > 0 && len >= kConsumerWarps;
                     }
                 }
             }
@@ -768,6 +741,45 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     // at kWarmBytes -- so that the producer's reads of them after its first
     // piece are L2 hits rather than dependent DRAM round trips.
     if (warp == kMergeWarp && range_lo < range_hi) {
+        // The first piece's first tiles (up to the ring's depth) and query
+        // rows, when the plan says so: lane j reads tile j's table entries and
+        // copies it into stage j, where the producer would have put it.
+        const int n_first = misc[kMiscEarly];
+        if (n_first > 0) {
+            const int s = first[0], gl = first[1];
+            const uint64_t policy = policy_evict_first();
+            if (lane == 0 && misc[kMiscEarly + 1]) {
+                mbar_arrive_expect_tx(qfull_bar(0), G * kDim * 2);
+                bulk_load(smem_u32(smem + kOffQ),
+                          p.q + (static_cast<size_t>(s) * p.num_q_heads + static_cast<size_t>(gl) * G) * kDim,
+                          G * kDim * 2, qfull_bar(0));
+            }
+            if (lane < n_first) {
+                const int32_t* row = p.block_tables + static_cast<size_t>(s) * p.max_blocks;
+                const int sk0 = skipped(s);
+                const int t = sk0 + first[2] + lane;  // the tile's index within the sequence
+                auto checked = [&](int bid) {
+                    if (bid < 0 || bid >= p.num_blocks) {
+                        if (p.err) atomicOr(p.err, PKV_DEVERR_BLOCK_ID);
+                        bid = 0;  // read a valid block instead; the output is flagged invalid
+                    }
+                    return bid;
+                };
+                int ya, yb = 0;
+                if constexpr (kBT >= kTok) {
+                    ya = (checked(__ldg(row + t / (kBT / kTok))) * Hkv + gl) * kBT + (t % (kBT / kTok)) * kTok;
+                } else {
+                    const int seq_blocks = (kTok * (sk0 + run_blocks(scan, s) - 1) + tail[s] + kBT - 1) / kBT;
+                    const int b0 = checked(__ldg(row + 2 * t));
+                    const int b1 = 2 * t + 1 < seq_blocks ? checked(__ldg(row + 2 * t + 1)) : b0;
+                    ya = (b0 * Hkv + gl) * kBT;
+                    yb = (b1 * Hkv + gl) * kBT;
+                }
+                mbar_arrive_expect_tx(full_bar(lane), kStageBytes);
+                issue_tile<kBT>(smem_u32(smem + kOffStages + lane * kStageBytes), &tm_k, &tm_v, ya, yb, full_bar(lane),
+                                policy);
+            }
+        }
         constexpr size_t kWarmBytes = 256 * 1024;
         const Cursor a = locate(scan, B, Hkv, range_lo);
         const Cursor z = locate(scan, B, Hkv, range_hi - 1);
@@ -813,17 +825,17 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     if (warp == kProducerWarp) {
         // ======================= producer warp =======================
         const uint64_t policy = policy_evict_first();
-        PieceWalk walk(scan, B, Hkv, range_lo, range_hi);
+        PieceWalk walk(scan, B, Hkv, range_lo, range_hi, first);
         Piece pc;
         int stage = 0, qslot = 0;
         uint32_t sphase = 0, qphase = 0;
         int tile = 0;  // position in the CTA's stream of tiles
         const int stop_at = (p.stop_tiles >= 0 && blockIdx.x == 0) ? p.stop_tiles : INT_MAX;
         int issued = 0, q_issued = 0;  // copies issued into the stage ring and the query ring
-        // Tiles [0, n_early) and, if q_early, the first query rows were
-        // copied during the plan: skipped here, counted in the drain.
-        const int n_early = misc[4];
-        bool q_early = misc[5] != 0;
+        // Tiles [0, n_early) and, if q_early, the first query rows are
+        // copied by the merge warp: skipped here, counted in the drain.
+        const int n_early = misc[kMiscEarly];
+        bool q_early = misc[kMiscEarly + 1] != 0;
         bool waited = false;  // griddep_wait done by this thread
         while (walk.next(pc)) {
             const int len = pc.len;
@@ -922,7 +934,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         // Lane l owns dims [4l, 4l + 4) of every head of the piece.
         const float NEG_INF = -INFINITY;
         const int d0 = lane * 4;
-        PieceWalk walk(scan, B, Hkv, range_lo, range_hi);
+        PieceWalk walk(scan, B, Hkv, range_lo, range_hi, first);
         Piece pc;
         int piece = 0;
         int gidx0 = 0;  // the CTA's block count before this piece, as the consumers count it
@@ -1159,7 +1171,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     // ========================= consumer warps =========================
     if constexpr (kFmaG > 0) {
         static_assert(kBT == kTok && !kSkip, "the CUDA-core variant serves the plain 16-token kernel");
-        fma_consumer_warp<kSlots, kFmaG>(p, smem, scan, tail, range_lo, range_hi, warp, lane, abort_flag, bar0);
+        fma_consumer_warp<kSlots, kFmaG>(p, smem, scan, tail, range_lo, range_hi, first, warp, lane, abort_flag, bar0);
         return;
     }
     const int r = lane >> 2;  // mma group id: token row / head column owner
@@ -1174,7 +1186,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     const int v_sw = lane & 7;
     const float NEG_INF = -INFINITY;
 
-    PieceWalk walk(scan, B, Hkv, range_lo, range_hi);
+    PieceWalk walk(scan, B, Hkv, range_lo, range_hi, first);
     Piece pc;
     int gidx0 = 0;
     int qslot = 0, piece = 0;
