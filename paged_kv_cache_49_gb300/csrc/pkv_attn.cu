@@ -251,7 +251,6 @@ pkv_status prepare(const void* q, const void* k_cache, const void* v_cache, cons
     prm.skip_tiles = nullptr;
     prm.side = nullptr;
     prm.stop_tiles = -1;
-    prm.early_issue = 0;
     L->grid = grid;
     L->slots = kc.slots;
     L->fn = kc.fn;
@@ -260,9 +259,7 @@ pkv_status prepare(const void* q, const void* k_cache, const void* v_cache, cons
 }
 
 // early: launch with programmatic stream serialization, so that the kernel's
-// prologue overlaps the previous kernel on the stream (see griddep_wait);
-// its first tile copies then wait for that kernel. Otherwise they may go out
-// during the plan.
+// prologue overlaps the previous kernel on the stream (see griddep_wait).
 pkv_status launch(const Launch& L, cudaStream_t stream, bool early) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(L.grid);
@@ -274,9 +271,7 @@ pkv_status launch(const Launch& L, cudaStream_t stream, bool early) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = early ? 1 : 0;
-    Params prm = L.prm;
-    prm.early_issue = early ? 0 : 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, L.fn, L.tm_k, L.tm_v, prm);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, L.fn, L.tm_k, L.tm_v, L.prm);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) {
         record_cuda_error(e);
@@ -1354,7 +1349,6 @@ extern "C" pkv_status pkv_attn_decode_static(const void* q, const void* k_cache,
     prm.skip_tiles = nullptr;
     prm.side = nullptr;
     prm.stop_tiles = -1;
-    prm.early_issue = 1;  // an ordinary launch: stream order covers earlier writes
 
     void* args[] = {&tm_k, &tm_v, &prm};
     e = cudaLaunchKernel(reinterpret_cast<const void*>(kc.fn), dim3(grid), dim3(attn::kThreads), args, kc.smem,

@@ -184,10 +184,6 @@ struct Params {
     // issues the copies of its first stop_tiles tiles and skips the rest, so
     // that a consumer's wait on the next one runs out.
     int stop_tiles;
-    // 1: the first piece's copies may be issued during the plan (the kernel
-    // was not launched behind kernels that write the KV cache); 0: only
-    // after griddep_wait, by the producer.
-    int early_issue;
 };
 
 // Position in the line of (sequence, KV head) block runs.
@@ -703,11 +699,12 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 // The walk's first piece is the part of the range in the run
                 // holding tile hi_t - 1 (run g, or the last tile of run g -
                 // 1). When that run is this sequence's, this thread records
-                // the piece, so that no warp searches for it, and, when the
-                // kernel may read the cache at once, how many of its tiles the
-                // merge warp (idle until the first piece ends) copies right
-                // after the plan: the producer's own first copies come several
-                // microseconds later, most of it cold instruction fetch.
+                // the piece, so that no warp searches for it, and how many of
+                // its tiles the merge warp (idle until the first piece ends)
+                // copies right after the plan (once the step's earlier kernels
+                // are done, when launched behind them): the producer's own
+                // first copies come several microseconds later, most of it cold
+                // instruction fetch.
                 if (nb > 0 && (r > 0 || g > 0)) {
                     const int gl = r > 0 ? g : g - 1;
                     const int seg = Hkv * before + gl * nb;  // the run's first tile
@@ -718,7 +715,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                         misc[kMiscFirst + 1] = gl;
                         misc[kMiscFirst + 2] = split - seg;
                         misc[kMiscFirst + 3] = split;
-                        int n = p.early_issue ? min(len, kStages) : 0;
+                        int n = min(len, kStages);
                         if (blockIdx.x == 0 && p.stop_tiles >= 0) n = min(n, p.stop_tiles);
                         misc[kMiscEarly] = n;
                         misc[kMiscEarly + 1] = n > 0 && len >= kConsumerWarps;
@@ -742,8 +739,11 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     // piece are L2 hits rather than dependent DRAM round trips.
     if (warp == kMergeWarp && range_lo < range_hi) {
         // The first piece's first tiles (up to the ring's depth) and query
-        // rows, when the plan says so: lane j reads tile j's table entries and
-        // copies it into stage j, where the producer would have put it.
+        // rows, when the plan found the piece: lane j reads tile j's table
+        // entries and copies it into stage j, where the producer would have
+        // put it. Only the tiles can hold what the step's earlier kernels
+        // (block copy, append) wrote: their copies wait for those kernels
+        // (a no-op for an ordinary launch).
         const int n_first = misc[kMiscEarly];
         if (n_first > 0) {
             const int s = first[0], gl = first[1];
@@ -754,7 +754,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                           p.q + (static_cast<size_t>(s) * p.num_q_heads + static_cast<size_t>(gl) * G) * kDim,
                           G * kDim * 2, qfull_bar(0));
             }
-            if (lane < n_first) {
+            const bool mine = lane < n_first;
+            int ya = 0, yb = 0;
+            if (mine) {
                 const int32_t* row = p.block_tables + static_cast<size_t>(s) * p.max_blocks;
                 const int sk0 = skipped(s);
                 const int t = sk0 + first[2] + lane;  // the tile's index within the sequence
@@ -765,7 +767,6 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                     }
                     return bid;
                 };
-                int ya, yb = 0;
                 if constexpr (kBT >= kTok) {
                     ya = (checked(__ldg(row + t / (kBT / kTok))) * Hkv + gl) * kBT + (t % (kBT / kTok)) * kTok;
                 } else {
@@ -775,6 +776,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                     ya = (b0 * Hkv + gl) * kBT;
                     yb = (b1 * Hkv + gl) * kBT;
                 }
+            }
+            griddep_wait();
+            if (mine) {
                 mbar_arrive_expect_tx(full_bar(lane), kStageBytes);
                 issue_tile<kBT>(smem_u32(smem + kOffStages + lane * kStageBytes), &tm_k, &tm_v, ya, yb, full_bar(lane),
                                 policy);
@@ -798,13 +802,14 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                                                   static_cast<size_t>(z.g + 1) * G) * kDim));
     }
 
-    // Everything above reads only inputs that the kernels of a decode step
-    // (block copy, append) do not write. Of what follows, only the
-    // producer's tile loads read what they wrote (the KV cache): the producer
-    // reads its first piece's query rows and table entries first, then waits
-    // for those kernels (when launched early) just before its first tile
-    // load. Every other thread waits here, so that the grid never completes
-    // before the kernels it was launched behind.
+    // Everything above but the merge warp's tile copies (which wait for
+    // them) reads only inputs that the kernels of a decode step (block copy,
+    // append) do not write. Of what follows, only the producer's tile loads
+    // read what they wrote (the KV cache): the producer reads its first
+    // piece's query rows and table entries first, then waits for those
+    // kernels (when launched early) just before its first tile load. Every
+    // other thread waits here, so that the grid never completes before the
+    // kernels it was launched behind.
     if (warp != kProducerWarp) griddep_wait();
 
     // Sequences with no context get a zero output row (sequence s by CTA
