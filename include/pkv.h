@@ -51,7 +51,7 @@ typedef int pkv_status;
 #define PKV_ERANGE (-3)      /* id or length outside the valid range */
 #define PKV_ECUDA (-4)       /* a CUDA runtime call failed */
 #define PKV_ENOSPC (-5)      /* append past the pages a sequence reserved */
-#define PKV_EUNSUPPORTED (-6) /* geometry this build does not handle */
+#define PKV_EUNSUPPORTED (-6) /* geometry the library does not handle */
 #define PKV_ESTATE (-7)      /* block manager found its own state inconsistent */
 
 /* Bits of the device-side error word. */
