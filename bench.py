@@ -669,7 +669,8 @@ def measure(pkv, name, args, rank, world, local, flush, e2e_on=True):
         "config": {"workload": w.name, "batch": B, "q_heads": w.num_q_heads, "kv_heads": w.num_kv_heads,
                    "head_dim": w.head_dim, "block_tokens": w.block_tokens, "context_tokens": int(ctx.sum()),
                    "pool_blocks": w.pool_blocks, "cow_pairs_per_step": sb.num_pairs,
-                   "num_ctas": args.num_ctas or pkv.default_ctas(B),
+                   "num_ctas": args.num_ctas or pkv.launch_ctas(B, w.num_kv_heads, int(sb.tables.shape[1]),
+                                                                 w.block_tokens),
                    "l2": "flushed before each timed launch (256 MiB write, then 256 MiB read: cold and clean)",
                    "parallelism": f"replicas x{world}"},
     }

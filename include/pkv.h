@@ -170,7 +170,10 @@ size_t pkv_attn_workspace_fixed_bytes(void);
  *   context_lens  : device int32 [num_seqs]
  *   num_ctas      : number of persistent CTAs (at most PKV_ATTN_MAX_CTAS, and
  *                   as many as the workspace holds partial slots for), 0 =
- *                   as many as fit at once on the device; the context of all
+ *                   as many as fit at once on the device, or fewer when the
+ *                   block tables bound the batch's work to under 4 tiles (16
+ *                   tokens of one KV head, plus 3 per sequence and KV head)
+ *                   per CTA; the context of all
  *                   (sequence, KV head) pairs is split evenly among them and
  *                   partial results of a pair split across CTAs are merged in
  *                   the same launch
@@ -373,10 +376,18 @@ pkv_status pkv_decode_step_host(const void* host_packed, void* device_staging, i
                                 void* device_out, void* host_out, uint32_t* device_error,
                                 void* stream);
 
-/* Number of persistent CTAs pkv_attn_decode launches for num_seqs sequences
- * when num_ctas == 0 (every CTA that fits on the current device at once);
- * 0 on error. */
+/* Number of persistent CTAs that fit on the current device at once for
+ * num_seqs sequences: the most pkv_attn_decode launches when num_ctas == 0
+ * (it launches fewer for a batch whose tables bound its work to a few tiles
+ * per CTA); 0 on error. */
 int pkv_attn_default_ctas(int num_seqs);
+
+/* Number of CTAs pkv_attn_decode / pkv_attn_decode_ex launch when num_ctas
+ * == 0, for num_seqs sequences, num_kv_heads KV heads, tables of
+ * max_blocks_per_seq entries and blocks of block_tokens tokens (8, 16, 32 or
+ * 64): pkv_attn_default_ctas(num_seqs), or fewer when the tables bound the
+ * batch's work to under 4 cost units per CTA. 0 on bad arguments. */
+int pkv_attn_launch_ctas(int num_seqs, int num_kv_heads, int max_blocks_per_seq, int block_tokens);
 
 /*
  * pkv_attn_decode_static -- pkv_attn_decode without a workspace argument, for

@@ -9,7 +9,7 @@ from ._native import (  # noqa: F401
     BLOCK_TOKENS, DEVERR_BLOCK_ID, DEVERR_CONTEXT, DEVERR_SLOT, DEVERR_TIMEOUT, EXPORTED,
     HEAD_DIM, LIB_PATH, MAX_CTAS, MAX_GROUP, AttentionWorkspace, BlockManager, Cascade, PkvError, PoolExhausted,
     ReservationExceeded, append, attn_decode, attn_decode_cuda_cores, attn_decode_static, block_copy, decode_step, decode_step_host,
-    default_ctas, new_error_word, step_layout,
+    default_ctas, launch_ctas, new_error_word, step_layout,
     read_device_error,
 )
 from .engine import (  # noqa: F401

@@ -44,6 +44,7 @@ EXPORTED = [
     "pkv_bm_newest_running", "pkv_bm_slots", "pkv_step_layout", "pkv_decode_step_host",
     "pkv_attn_cascade_workspace_size", "pkv_cascade_staging_size", "pkv_cascade_plan", "pkv_attn_decode_cascade",
     "pkv_attn_decode_wait_test", "pkv_attn_decode_cuda_cores", "pkv_attn_workspace_fixed_bytes",
+    "pkv_attn_launch_ctas",
 ]
 BLOCK_SIZES = (8, 16, 32, 64)
 
@@ -105,6 +106,7 @@ def _load() -> ctypes.CDLL:
         "pkv_attn_workspace_fixed_bytes": (sz, []),
         "pkv_attn_decode": (i32, [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, f32, i32, vp, sz, vp, vp]),
         "pkv_attn_default_ctas": (i32, [i32]),
+        "pkv_attn_launch_ctas": (i32, [i32, i32, i32, i32]),
         "pkv_attn_decode_cuda_cores": (i32, [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, f32, i32, vp, sz, vp,
                                              vp]),
         "pkv_attn_decode_wait_test": (i32, [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, f32, i32, vp, sz, vp,
@@ -239,6 +241,11 @@ def block_copy(k_cache, v_cache, pairs, device_error=None, stream=None) -> None:
 
 def default_ctas(num_seqs: int) -> int:
     return int(_lib.pkv_attn_default_ctas(num_seqs))
+
+
+def launch_ctas(num_seqs: int, num_kv_heads: int, max_blocks_per_seq: int, block_tokens: int = BLOCK_TOKENS) -> int:
+    """CTAs attn_decode launches with num_ctas = 0 for this batch shape."""
+    return int(_lib.pkv_attn_launch_ctas(num_seqs, num_kv_heads, max_blocks_per_seq, block_tokens))
 
 
 class AttentionWorkspace:

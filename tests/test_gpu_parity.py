@@ -284,3 +284,15 @@ def test_one_workspace_serves_any_launch_shape(pkv):
         assert ws.read_error() == 0
         assert not ws.tensor[4:counters_end].any(), "counters left nonzero"
         _close(out, sh["ref"])
+
+
+def test_default_grid_follows_the_tables_bound(pkv):
+    """With num_ctas = 0 a batch whose block tables bound its work to under
+    4 cost units per CTA (tiles plus 3 per sequence and KV head, every row
+    full) launches fewer CTAs than fit; larger batches launch every CTA."""
+    assert pkv.launch_ctas(4, 8, 13) == min(pkv.default_ctas(4), -(-8 * 4 * (13 + 3) // 4))
+    assert pkv.launch_ctas(6, 1, 33) == min(pkv.default_ctas(6), -(-6 * (33 + 3) // 4))
+    assert pkv.launch_ctas(64, 8, 512) == pkv.default_ctas(64)
+    assert pkv.launch_ctas(8, 8, 145) == pkv.default_ctas(8)
+    assert pkv.launch_ctas(4, 8, 26, 8) == pkv.launch_ctas(4, 8, 13, 16)  # the bound counts 16-token tiles
+    assert pkv.launch_ctas(4, 8, 13, 12) == 0  # an unsupported block size
