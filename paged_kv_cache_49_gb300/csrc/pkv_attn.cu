@@ -41,30 +41,20 @@ EncodeTiledFn encode_fn() {
 }
 
 // View of a cache as token rows (num_blocks * Hkv * block_tokens rows of 128
-// bf16). Blocks of 16 tokens or more: 3-D, {64 columns, rows, 2 column
-// halves} with the halves 128 bytes apart, so that one box of {64, 16, 2}
-// brings 16 rows of one (block, KV head) -- 4 KB -- laid out in shared memory
-// as the two 16 x 64 halves one after the other, each in the 128-byte
-// swizzle. 8-token blocks: 2-D, {64 columns, rows}, boxes of 64 x 8 (a tile
-// takes two blocks).
+// bf16), 3-D: {64 columns, rows, 2 column halves} with the halves 128 bytes
+// apart, so that one box of {64, min(16, block tokens), 2} brings that many
+// rows of one (block, KV head) -- 4 KB, or 2 KB for 8-token blocks -- laid out
+// in shared memory as the two halves one after the other, each in the
+// 128-byte swizzle.
 bool make_cache_map(CUtensorMap* map, const void* base, int num_blocks, int hkv, int block_tokens) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
     const cuuint64_t rows = static_cast<cuuint64_t>(num_blocks) * hkv * block_tokens;
-    if (block_tokens >= kTok) {
-        cuuint64_t dims[3] = {64, rows, 2};
-        cuuint64_t strides[2] = {static_cast<cuuint64_t>(kDim) * 2, 128};
-        cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kTok), 2};
-        cuuint32_t estr[3] = {1, 1, 1};
-        return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-    }
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(kDim), rows};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(kDim) * 2};
-    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(block_tokens)};
-    cuuint32_t estr[2] = {1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+    cuuint64_t dims[3] = {64, rows, 2};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(kDim) * 2, 128};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(block_tokens < kTok ? block_tokens : kTok), 2};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

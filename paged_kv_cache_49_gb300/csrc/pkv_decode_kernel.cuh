@@ -84,6 +84,18 @@ constexpr int kPieceCost = 3;
 constexpr int kMergeGroup = 8;
 constexpr int kHalfBytes = kTok * 64 * 2;  // one 16 x 64 bf16 box
 constexpr int kBlockBytes = 2 * kHalfBytes;  // one K (or V) block of one KV head
+// A stage's K (and V) tile in shared memory: 16 token rows of two 64-column
+// halves, each row 128 bytes in the 128-byte swizzle, in atoms of 8 rows of
+// one half. With blocks of 16 tokens or more the halves are 2 KB apart and
+// the two 8-row atoms of a half adjacent (one box: both halves of 16 rows);
+// with 8-token blocks the rows 0-7 and 8-15 come from two blocks, one box
+// each ({64, 8, 2}: both halves of 8 rows), so there the 8-row groups are 2
+// KB apart and the halves adjacent.
+template <int kBT>
+struct TileLayout {
+    static constexpr uint32_t kHalf = kBT >= kTok ? kHalfBytes : kHalfBytes / 2;   // between the halves
+    static constexpr uint32_t kRows8 = kBT >= kTok ? kHalfBytes / 2 : kHalfBytes;  // between rows 0-7 and 8-15
+};
 constexpr int kStageBytes = 2 * kBlockBytes;
 constexpr int kQBytes = kMaxG * kDim * 2;
 constexpr int kORow = 132;  // floats per head row of merge buffers and partials
@@ -541,24 +553,16 @@ __device__ __forceinline__ void fma_consumer_warp(const Params& p, uint8_t* smem
 // of their math compiled for that group size (16-token blocks only).
 // One tile's copies into a stage: K then V, 16 token rows each as one box
 // of both 64-column halves (blocks of 16 tokens or more), or, with 8-token
-// blocks, as 16 x 64 halves whose rows 0-7 come from the block at ya and rows
-// 8-15 from the block at yb.
+// blocks, as two boxes of 8 rows and both halves, rows 0-7 from the block at
+// ya and rows 8-15 from the block at yb (TileLayout).
 template <int kBT>
 __device__ __forceinline__ void issue_tile(uint32_t dst, const CUtensorMap* tm_k, const CUtensorMap* tm_v, int ya,
                                            int yb, uint32_t fb, uint64_t policy) {
-    if constexpr (kBT >= kTok) {
-        tma_load_3d(dst, tm_k, 0, ya, 0, fb, policy);
-        tma_load_3d(dst + kBlockBytes, tm_v, 0, ya, 0, fb, policy);
-    } else {
-        constexpr uint32_t kRow8 = 8 * 128;
-        tma_load_2d(dst, tm_k, 0, ya, fb, policy);
-        tma_load_2d(dst + kRow8, tm_k, 0, yb, fb, policy);
-        tma_load_2d(dst + kHalfBytes, tm_k, 64, ya, fb, policy);
-        tma_load_2d(dst + kHalfBytes + kRow8, tm_k, 64, yb, fb, policy);
-        tma_load_2d(dst + kBlockBytes, tm_v, 0, ya, fb, policy);
-        tma_load_2d(dst + kBlockBytes + kRow8, tm_v, 0, yb, fb, policy);
-        tma_load_2d(dst + kBlockBytes + kHalfBytes, tm_v, 64, ya, fb, policy);
-        tma_load_2d(dst + kBlockBytes + kHalfBytes + kRow8, tm_v, 64, yb, fb, policy);
+    tma_load_3d(dst, tm_k, 0, ya, 0, fb, policy);
+    tma_load_3d(dst + kBlockBytes, tm_v, 0, ya, 0, fb, policy);
+    if constexpr (kBT < kTok) {
+        tma_load_3d(dst + TileLayout<kBT>::kRows8, tm_k, 0, yb, 0, fb, policy);
+        tma_load_3d(dst + kBlockBytes + TileLayout<kBT>::kRows8, tm_v, 0, yb, 0, fb, policy);
     }
 }
 
@@ -1183,11 +1187,12 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     const int c = lane & 3;   // thread in group
     const uint32_t stage_base = smem_u32(smem + kOffStages);
     // ldmatrix address pieces (row of the 16 x 16 tile each lane points at)
-    const uint32_t k_row_off = static_cast<uint32_t>(lane & 15) * 128u;
+    using TL = TileLayout<kBT>;
+    const uint32_t k_row_off = static_cast<uint32_t>((lane & 15) >> 3) * TL::kRows8 + static_cast<uint32_t>(lane & 7) * 128u;
     const int k_sw = lane & 7;
     const int k_hi = lane >> 4;
     const int v_mat = lane >> 3;
-    const uint32_t v_row_off = static_cast<uint32_t>((lane & 7) + ((v_mat >> 1) << 3)) * 128u;
+    const uint32_t v_row_off = static_cast<uint32_t>(v_mat >> 1) * TL::kRows8 + static_cast<uint32_t>(lane & 7) * 128u;
     const int v_sw = lane & 7;
     const float NEG_INF = -INFINITY;
 
@@ -1269,7 +1274,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             for (int ks = 0; ks < 8; ++ks) {
                 const int chunk = ((ks & 3) << 1) | k_hi;
                 uint32_t a[4];
-                ldmatrix_x4(a, sk + (ks >> 2) * kHalfBytes + k_row_off + ((chunk ^ k_sw) << 4));
+                ldmatrix_x4(a, sk + (ks >> 2) * TL::kHalf + k_row_off + ((chunk ^ k_sw) << 4));
                 if (ks & 1) mma_bf16_16816(sb, a, qb[2 * ks], qb[2 * ks + 1]);
                 else mma_bf16_16816(sa, a, qb[2 * ks], qb[2 * ks + 1]);
             }
@@ -1313,7 +1318,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             for (int j = 0; j < 8; ++j) {
                 const int chunk = ((j & 3) << 1) | (v_mat & 1);
                 uint32_t a[4];
-                ldmatrix_x4_trans(a, sv + (j >> 2) * kHalfBytes + v_row_off + ((chunk ^ v_sw) << 4));
+                ldmatrix_x4_trans(a, sv + (j >> 2) * TL::kHalf + v_row_off + ((chunk ^ v_sw) << 4));
                 a[0] &= vmask01;
                 a[1] &= vmask01;
                 a[2] &= vmask23;

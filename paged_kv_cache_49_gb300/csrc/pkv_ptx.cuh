@@ -96,15 +96,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 }
 
 // ---- TMA ---------------------------------------------------------------------
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int x, int y,
-                                            uint32_t bar, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-        "l"(tmap), "r"(x), "r"(y), "r"(bar), "l"(policy)
-        : "memory");
-}
-
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int x, int y, int z,
                                             uint32_t bar, uint64_t policy) {
     asm volatile(
